@@ -1,0 +1,224 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: a paged KV cache for single-token decode
+ * attention on one GB300 (sm_103a).
+ *
+ * Sources the operations restate (web pages, by title and section):
+ *   [A] "无 vLLM 环境下的 Paged-KV 与连续批处理调度" (mixtureofinsights.com)
+ *   [B] "vLLM核心概念：PagedAttention、Continuous Batching、KV Cache等原理" (5688vip.com, ch. 3)
+ *   [C] "离开 N 卡后的真实世界：Ultra x7 358h 平台上的 TTS 推理框架重构" (mixtureofinsights.com)
+ *   [D] "连续批处理与KV缓存" (5688vip.com, course ch. 4)
+ *   [E] "轻量级推理引擎实战：KV Cache 量化与连续批处理的底层优化" (lpnh.cn)
+ *
+ * Conventions
+ *   - Every function returns an int status (PKV_OK or a negative PKV_ERR_*),
+ *     except the two size queries and the allocator constructor.
+ *   - Host functions (allocator, tables) touch only host memory and are not
+ *     thread-safe: callers serialise access to one allocator.
+ *   - Device functions enqueue kernels on the given CUDA stream (a
+ *     cudaStream_t passed as void*; NULL = legacy default stream) and return
+ *     without synchronising. They validate their scalar arguments and pointer
+ *     alignment on the host and return PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED
+ *     without launching anything; PKV_ERR_CUDA reports a launch failure.
+ *     Values that live in device memory (block ids, slots, context lengths)
+ *     are checked inside the kernels: an out-of-range value is skipped (no
+ *     memory access is made with it) and, if the descriptor carries an error
+ *     word, a PKV_DEVERR_* bit is OR-ed into it.
+ *   - All device buffers are owned by the caller. No device function
+ *     allocates memory. bf16 data is passed as raw 16-bit words.
+ *
+ * Layout (all row-major, per layer):
+ *   k_pool, v_pool  [num_blocks][Hkv][block_size][head_dim]  bf16 or int8
+ *   scales          [num_blocks][Hkv][2] fp32 (INT8 only; [..][0] = K, [..][1] = V)
+ *   k_tail, v_tail  [max_slots][Hkv][block_size][head_dim] bf16 (INT8 only)
+ *   block tables    [B][max_blocks] int32, logical block -> physical block, -1 pad
+ *   q, out          [B][Hq][head_dim] bf16
+ *   query head h reads kv head h / (Hq / Hkv).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define PKV_OK                 0
+#define PKV_ERR_INVALID       -1  /* null pointer, bad size or alignment */
+#define PKV_ERR_OOM           -2  /* not enough free blocks; nothing changed */
+#define PKV_ERR_NOT_FOUND     -3  /* request id is not live */
+#define PKV_ERR_EXISTS        -4  /* request id is already live */
+#define PKV_ERR_UNSUPPORTED   -5  /* shape outside the compiled set (see below) */
+#define PKV_ERR_CUDA          -6  /* a CUDA runtime call failed */
+
+/* bits a kernel ORs into the descriptor's error word */
+#define PKV_DEVERR_BLOCK_ID    1  /* block id < 0 or >= num_blocks */
+#define PKV_DEVERR_SLOT        2  /* slot < 0 or >= max_slots */
+#define PKV_DEVERR_CTX_LEN     4  /* context length < 0 or > max_blocks * block_size */
+#define PKV_DEVERR_OFFSET      8  /* in-block offset < 0 or >= block_size */
+#define PKV_DEVERR_TIMEOUT    16  /* a bounded wait on an asynchronous copy expired */
+
+#define PKV_DTYPE_BF16 0
+#define PKV_DTYPE_INT8 1
+
+/* Compiled shapes: head_dim in {64, 128}; block_size in {16, 64};
+ * Hq / Hkv in {1, 2, 4} for head_dim 128 and {1, 2, 4, 8} for head_dim 64. */
+
+/* ======================================================================== */
+/* Host block allocator ([D] §4.2; [A] §1.2; [B] §3.2; [E] §2.1)            */
+/* ======================================================================== */
+
+/* A FIFO pool of block ids: allocations take ids from the front, frees
+ * return them to the back, each in O(1) per block ([D] §4.2's free-block pool).
+ * Each live request owns an ordered list of private blocks, optionally
+ * preceded by shared blocks (a common prompt prefix, [B] §3.2) that it
+ * references but does not own. */
+typedef struct pkv_allocator pkv_allocator;
+
+/* Creates a pool of num_blocks ids. initial_order (nullable, num_blocks
+ * entries, a permutation of 0..num_blocks-1) sets the initial free-list
+ * order, e.g. a shuffled pool; NULL means 0, 1, 2, ... block_size is
+ * recorded for the caller's arithmetic. Returns NULL on invalid arguments or
+ * host allocation failure. The handle owns only host memory. */
+pkv_allocator* pkv_allocator_create(int32_t num_blocks, int32_t block_size,
+                                    const int32_t* initial_order);
+void pkv_allocator_destroy(pkv_allocator* a);
+
+/* All-or-nothing allocation of n_blocks >= 0 private blocks for a new
+ * request ([D] §4.2 "allocate"): writes the ids, in order, to out_ids
+ * (n_blocks entries; may be NULL when n_blocks == 0).
+ * PKV_ERR_OOM if fewer are free (pool unchanged); PKV_ERR_EXISTS if req_id is
+ * live (the page's sketch would silently overwrite it and leak its blocks). */
+int pkv_alloc(pkv_allocator* a, int64_t req_id, int32_t n_blocks, int32_t* out_ids);
+
+/* One more block at the end of a live request's list ([D] §4.2
+ * "append_block"; [E] §2.1 on-demand allocation). PKV_ERR_OOM when the pool
+ * is empty ("wait"), PKV_ERR_NOT_FOUND for an unknown request. */
+int pkv_append_block(pkv_allocator* a, int64_t req_id, int32_t* out_id);
+
+/* Returns the request's private blocks to the back of the free list in the
+ * order it held them and forgets the request ([D] §4.2 "free").
+ * PKV_ERR_NOT_FOUND (no change) for an unknown request. */
+int pkv_free(pkv_allocator* a, int64_t req_id);
+
+/* Puts n shared block ids in front of a live request's table. They are
+ * never returned by pkv_free; their owner (the request that allocated them)
+ * frees them. No check is made that the ids are live. */
+int pkv_attach_shared(pkv_allocator* a, int64_t req_id, const int32_t* ids, int32_t n);
+
+/* Number of free blocks; -1 for a NULL handle. */
+int pkv_num_free(const pkv_allocator* a);
+
+/* Writes up to cap ids of the request's table (shared then private) to out
+ * (nullable when cap == 0) and returns the table length, or a negative
+ * status. */
+int pkv_request_table(const pkv_allocator* a, int64_t req_id, int32_t* out, int32_t cap);
+
+/* Writes up to cap ids of the free list, front first, and returns its length. */
+int pkv_free_list(const pkv_allocator* a, int32_t* out, int32_t cap);
+
+/* Block tables for B requests: out_table[B][max_blocks] (host memory), each
+ * row the request's table padded with -1 ([B] §3.2, [E] §2.1 "Block Table").
+ * PKV_ERR_NOT_FOUND for an unknown request, PKV_ERR_INVALID if a table is
+ * longer than max_blocks; out_table is then unspecified. */
+int pkv_build_block_tables(const pkv_allocator* a, const int64_t* req_ids, int32_t B,
+                           int32_t max_blocks, int32_t* out_table);
+
+/* ======================================================================== */
+/* Device side                                                             */
+/* ======================================================================== */
+
+/* One layer's cache. Pools and tails must be 16-byte aligned. In BF16 mode
+ * scales, k_tail and v_tail are unused (may be NULL) and max_slots may be 0.
+ * err_word (nullable) is a device int32 the kernels OR PKV_DEVERR_* bits into. */
+typedef struct pkv_cache_desc {
+    void*    k_pool;
+    void*    v_pool;
+    float*   scales;
+    void*    k_tail;
+    void*    v_tail;
+    int32_t  num_blocks;
+    int32_t  num_q_heads;
+    int32_t  num_kv_heads;
+    int32_t  head_dim;
+    int32_t  block_size;
+    int32_t  max_slots;
+    int32_t  dtype;          /* PKV_DTYPE_BF16 or PKV_DTYPE_INT8 */
+    int32_t* err_word;
+} pkv_cache_desc;
+
+/* Per-step append ([D] §4.2 "expand: a request that generates a new token
+ * appends to its cache"; [E] §2.1). Writes the T new rows k[T][Hkv][d],
+ * v[T][Hkv][d] (device, bf16) of token t at in-block offset offsets[t]:
+ *   BF16 mode: into pool block block_ids[t];
+ *   INT8 mode: into the bf16 tail of sequence slot slots[t] (the block is
+ *              quantized into the pool once it fills, see below).
+ * block_ids (BF16) / slots (INT8) and offsets are device int32 [T]; the
+ * unused one may be NULL. T == 0 is a no-op. */
+int pkv_append_kv(const pkv_cache_desc* c, const void* k, const void* v,
+                  const int32_t* block_ids, const int32_t* offsets, const int32_t* slots,
+                  int32_t T, void* stream);
+
+/* Quantize-on-fill ([E] §3 quantize_block, granularity per
+ * (block, kv_head, K|V)): for each m < M, quantizes the full bf16 tail of
+ * slot slots[m] into pool block block_ids[m] and writes its scales:
+ *   s = max|x| / 127 (fp32 IEEE division), or 1.0 if max|x| < 1e-6;
+ *   q = clamp(round_half_even(x / s), -127, 127) (fp32 IEEE division).
+ * The bytes and scales are a deterministic function of the tail's bf16
+ * values. INT8 mode only. block_ids, slots: device int32 [M]; an entry whose
+ * block id is -1 is skipped, so a fixed-size list may be padded (e.g. one
+ * entry per running sequence, -1 where no block filled this step). */
+int pkv_quantize_full_blocks(const pkv_cache_desc* c, const int32_t* block_ids,
+                             const int32_t* slots, int32_t M, void* stream);
+
+/* Same quantization with a caller-given source instead of a tail: block m
+ * takes rows m*block_size .. m*block_size+block_size-1 of k_src / v_src
+ * ([M*block_size][Hkv][d] bf16, device) -- e.g. the full blocks of a prompt.
+ * INT8 mode only. */
+int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const void* v_src,
+                             const int32_t* block_ids, int32_t M, void* stream);
+
+/* Decode attention ([B] §3.1 one new query against all cached K, V;
+ * [E] §1 each decode step reads the whole cache; [A] §2 GQA; [C] §2 tiled
+ * softmax in on-chip memory). For each sequence b < B and query head h:
+ *   out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . k_t) v_t
+ * over the ctx_lens[b] tokens t of sequence b, where token t lives in block
+ * block_tables[b][t / bs] at offset t % bs, dequantized as q * scale in INT8
+ * mode -- except that in INT8 mode the last ctx_lens[b] % bs tokens (the
+ * partly filled block) are read from the bf16 tail of slot slots[b].
+ * Accumulation is fp32; out is bf16. ctx_lens[b] == 0 gives a zero row.
+ *
+ * split_tokens == 0: one pass per (b, kv_head); ws_o, ws_ml unused (NULL ok).
+ * split_tokens > 0 (a multiple of block_size and of 16): the context is cut
+ *   into chunks of split_tokens tokens, computed independently into the
+ *   caller's workspace, then merged by the split-K reduce (same stream).
+ *   Needs max_splits * split_tokens >= max_blocks * block_size and
+ *   ws_o  >= pkv_splitk_ws_o_bytes(B, Hq, d, max_splits),
+ *   ws_ml >= pkv_splitk_ws_ml_bytes(B, Hq, max_splits), 16-byte aligned.
+ * slots may be NULL in BF16 mode. */
+int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
+                         int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
+                         int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
+                         float* ws_o, float* ws_ml, void* out, void* stream);
+
+/* Split-K merge of partial softmax states (the combination rule of a
+ * softmax over a partition of the context; the pages' tiled softmax, [C] §2).
+ * ws_o [B][Hq][max_splits][d] and ws_ml [B][Hq][max_splits][2] fp32 hold,
+ * for split j < ceil(ctx_lens[b] / split_tokens): m_j, l_j and
+ * o_j = sum_t 2^(x_t - m_j) v_t with x_t = log2(e) * sm_scale * q . k_t
+ * (so m is in log2 units) and l_j = sum_t 2^(x_t - m_j). Writes
+ *   out[b][h] = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j
+ * as bf16 (a zero row when ctx_lens[b] == 0). */
+int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_lens,
+                      int32_t B, int32_t Hq, int32_t head_dim, int32_t split_tokens,
+                      int32_t max_splits, void* out, void* stream);
+
+size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits);
+size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

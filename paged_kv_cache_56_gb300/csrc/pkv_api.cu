@@ -1,0 +1,376 @@
+// C ABI of libpkv.so: argument validation and kernel launches for the
+// append, quantize-on-fill, decode-attention and split-K-merge entry points
+// declared in include/pkv.h. Every entry point launches on the caller's
+// stream and never allocates device memory.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/pkv.h"
+#include "kernels.cuh"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Append: one 16-byte chunk of one (token, K|V, kv head) row per thread.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) append_kernel(const uint16_t* __restrict__ k,
+                                                     const uint16_t* __restrict__ v,
+                                                     const int32_t* __restrict__ block_ids,
+                                                     const int32_t* __restrict__ offsets,
+                                                     const int32_t* __restrict__ slots, int32_t T,
+                                                     int32_t Hkv, int32_t bs, int32_t num_blocks,
+                                                     int32_t max_slots, int int8_mode, void* k_dst,
+                                                     void* v_dst, int32_t* err) {
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t rows = int64_t(T) * 2 * Hkv;
+    if (e >= rows * CH) return;
+    const int64_t r = e / CH;
+    const int c = int(e % CH);
+    const int t = int(r / (2 * Hkv));
+    const int kv = int((r / Hkv) % 2);
+    const int h = int(r % Hkv);
+    const int off = offsets[t];
+    if (off < 0 || off >= bs) {
+        if (c == 0) report(err, kErrOffset);
+        return;
+    }
+    int64_t row;
+    if (int8_mode) {
+        const int s = slots[t];
+        if (s < 0 || s >= max_slots) {
+            if (c == 0) report(err, kErrSlot);
+            return;
+        }
+        row = (int64_t(s) * Hkv + h) * bs + off;
+    } else {
+        const int blk = block_ids[t];
+        if (blk < 0 || blk >= num_blocks) {
+            if (c == 0) report(err, kErrBlockId);
+            return;
+        }
+        row = (int64_t(blk) * Hkv + h) * bs + off;
+    }
+    const uint16_t* src = (kv ? v : k) + (int64_t(t) * Hkv + h) * D + c * 8;
+    uint16_t* dst = static_cast<uint16_t*>(kv ? v_dst : k_dst) + row * D + c * 8;
+    *reinterpret_cast<uint4*>(dst) = ldg128(src);
+}
+
+// ---------------------------------------------------------------------------
+// Quantize: one warp per (block m, kv head, K|V) slab of bs x D bf16 values.
+//   scale = max|x| / 127 (IEEE fp32 division), 1.0 if max|x| < 1e-6;
+//   q = clamp(rint(x / scale), -127, 127), IEEE fp32 division, ties to even.
+// The source slab is rows [bs] with a row stride (elements) and a base.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) quantize_kernel(const uint16_t* __restrict__ k_src,
+                                                       const uint16_t* __restrict__ v_src,
+                                                       int from_tail, const int32_t* __restrict__ block_ids,
+                                                       const int32_t* __restrict__ slots, int32_t M,
+                                                       int32_t Hkv, int32_t bs, int32_t num_blocks,
+                                                       int32_t max_slots, int8_t* k_pool, int8_t* v_pool,
+                                                       float* scales, int32_t* err) {
+    constexpr int CH = D / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t slab = int64_t(blockIdx.x) * 4 + warp;
+    if (slab >= int64_t(M) * 2 * Hkv) return;
+    const int m = int(slab / (2 * Hkv));
+    const int kv = int((slab / Hkv) % 2);
+    const int h = int(slab % Hkv);
+    const int blk = block_ids[m];
+    if (blk == -1) return;  // padding entry of a fixed-size list
+    if (blk < 0 || blk >= num_blocks) {
+        if (lane == 0) report(err, kErrBlockId);
+        return;
+    }
+    const uint16_t* base;
+    int64_t row_stride;
+    if (from_tail) {
+        const int s = slots[m];
+        if (s < 0 || s >= max_slots) {
+            if (lane == 0) report(err, kErrSlot);
+            return;
+        }
+        base = (kv ? v_src : k_src) + (int64_t(s) * Hkv + h) * bs * D;
+        row_stride = D;
+    } else {
+        base = (kv ? v_src : k_src) + (int64_t(m) * bs * Hkv + h) * D;
+        row_stride = int64_t(Hkv) * D;
+    }
+    const int nch = bs * CH;
+    float mx = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+        const uint4 w = ldg128(base + int64_t(c / CH) * row_stride + (c % CH) * 8);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f2(ws[i]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float scale = mx < 1e-6f ? 1.0f : __fdiv_rn(mx, 127.0f);
+    int8_t* dst = (kv ? v_pool : k_pool) + (int64_t(blk) * Hkv + h) * bs * D;
+    for (int c = lane; c < nch; c += 32) {
+        const uint4 w = ldg128(base + int64_t(c / CH) * row_stride + (c % CH) * 8);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f2(ws[i]);
+            int q0 = __float2int_rn(__fdiv_rn(f.x, scale));
+            int q1 = __float2int_rn(__fdiv_rn(f.y, scale));
+            q0 = min(127, max(-127, q0));
+            q1 = min(127, max(-127, q1));
+            const uint32_t pair = (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8);
+            packed[i >> 1] |= pair << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint2*>(dst + int64_t(c) * 8) = make_uint2(packed[0], packed[1]);
+    }
+    if (lane == 0) scales[(int64_t(blk) * Hkv + h) * 2 + kv] = scale;
+}
+
+// ---------------------------------------------------------------------------
+// Host helpers
+// ---------------------------------------------------------------------------
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_desc(const pkv_cache_desc* c) {
+    if (!c || !c->k_pool || !c->v_pool) return PKV_ERR_INVALID;
+    if (!aligned16(c->k_pool) || !aligned16(c->v_pool)) return PKV_ERR_INVALID;
+    if (c->num_blocks <= 0 || c->num_q_heads <= 0 || c->num_kv_heads <= 0) return PKV_ERR_INVALID;
+    if (c->dtype != PKV_DTYPE_BF16 && c->dtype != PKV_DTYPE_INT8) return PKV_ERR_INVALID;
+    if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (c->block_size != 16 && c->block_size != 64) return PKV_ERR_UNSUPPORTED;
+    if (c->num_q_heads % c->num_kv_heads) return PKV_ERR_UNSUPPORTED;
+    const int g = c->num_q_heads / c->num_kv_heads;
+    const bool g_ok = g == 1 || g == 2 || g == 4 || (g == 8 && c->head_dim == 64);
+    if (!g_ok) return PKV_ERR_UNSUPPORTED;
+    if (c->dtype == PKV_DTYPE_INT8) {
+        if (!c->scales || !c->k_tail || !c->v_tail || c->max_slots <= 0) return PKV_ERR_INVALID;
+        if (!aligned16(c->k_tail) || !aligned16(c->v_tail) ||
+            (reinterpret_cast<uintptr_t>(c->scales) & 7u))
+            return PKV_ERR_INVALID;
+    }
+    return PKV_OK;
+}
+
+static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+template <int D, int G, bool INT8, bool SPLIT>
+static int launch_decode_t(const DecodeParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+    auto fn = decode_kernel<D, G, INT8, SPLIT>;
+    static int configured[64] = {0};  // per device: largest dynamic smem set so far
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+    if (int(smem) > configured[dev]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured[dev] = int(smem);
+    }
+    fn<<<grid, kThreads, smem, st>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int D, bool INT8, bool SPLIT>
+static int dispatch_g(int g, const DecodeParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+    switch (g) {
+        case 1: return launch_decode_t<D, 1, INT8, SPLIT>(p, grid, smem, st);
+        case 2: return launch_decode_t<D, 2, INT8, SPLIT>(p, grid, smem, st);
+        case 4: return launch_decode_t<D, 4, INT8, SPLIT>(p, grid, smem, st);
+        case 8:
+            if constexpr (D == 64) return launch_decode_t<D, 8, INT8, SPLIT>(p, grid, smem, st);
+            return PKV_ERR_UNSUPPORTED;
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+}
+
+static size_t decode_smem(int d, int g, bool int8, int tab_cap) {
+    size_t fixed = 0;
+    const size_t gd = size_t(g);
+    if (d == 64) fixed = int8 ? decode_smem_fixed<64, 1, true>() : decode_smem_fixed<64, 1, false>();
+    else fixed = int8 ? decode_smem_fixed<128, 1, true>() : decode_smem_fixed<128, 1, false>();
+    // decode_smem_fixed<.., G=1, ..> counts one head of merge space; add the rest
+    fixed += size_t(kWarps) * (gd - 1) * (size_t(d) * 4 + 8);
+    return fixed + size_t(tab_cap) * (int8 ? 12 : 4);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits) {
+    if (B < 0 || Hq < 0 || head_dim < 0 || max_splits < 0) return 0;
+    return size_t(B) * size_t(Hq) * size_t(max_splits) * size_t(head_dim) * sizeof(float);
+}
+
+size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits) {
+    if (B < 0 || Hq < 0 || max_splits < 0) return 0;
+    return size_t(B) * size_t(Hq) * size_t(max_splits) * 2 * sizeof(float);
+}
+
+int pkv_append_kv(const pkv_cache_desc* c, const void* k, const void* v, const int32_t* block_ids,
+                  const int32_t* offsets, const int32_t* slots, int32_t T, void* stream) {
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (T < 0) return PKV_ERR_INVALID;
+    if (T == 0) return PKV_OK;
+    if (!k || !v || !offsets || !aligned16(k) || !aligned16(v)) return PKV_ERR_INVALID;
+    const bool int8 = c->dtype == PKV_DTYPE_INT8;
+    if (int8 ? !slots : !block_ids) return PKV_ERR_INVALID;
+    const int64_t total = int64_t(T) * 2 * c->num_kv_heads * (c->head_dim / 8);
+    const int64_t grid = (total + 255) / 256;
+    if (grid > 0x7FFFFFFF) return PKV_ERR_INVALID;
+    void* kd = int8 ? c->k_tail : c->k_pool;
+    void* vd = int8 ? c->v_tail : c->v_pool;
+    auto s = static_cast<cudaStream_t>(stream);
+    const auto* kk = static_cast<const uint16_t*>(k);
+    const auto* vv = static_cast<const uint16_t*>(v);
+    if (c->head_dim == 128)
+        append_kernel<128><<<unsigned(grid), 256, 0, s>>>(kk, vv, block_ids, offsets, slots, T, c->num_kv_heads,
+                                                          c->block_size, c->num_blocks, c->max_slots, int8, kd,
+                                                          vd, c->err_word);
+    else
+        append_kernel<64><<<unsigned(grid), 256, 0, s>>>(kk, vv, block_ids, offsets, slots, T, c->num_kv_heads,
+                                                         c->block_size, c->num_blocks, c->max_slots, int8, kd,
+                                                         vd, c->err_word);
+    return cuda_status(cudaGetLastError());
+}
+
+static int quantize_common(const pkv_cache_desc* c, const void* k_src, const void* v_src, int from_tail,
+                           const int32_t* block_ids, const int32_t* slots, int32_t M, void* stream) {
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (c->dtype != PKV_DTYPE_INT8 || M < 0) return PKV_ERR_INVALID;
+    if (M == 0) return PKV_OK;
+    if (!block_ids || (from_tail && !slots) || !k_src || !v_src || !aligned16(k_src) || !aligned16(v_src))
+        return PKV_ERR_INVALID;
+    const int64_t slabs = int64_t(M) * 2 * c->num_kv_heads;
+    const int64_t grid = (slabs + 3) / 4;
+    if (grid > 0x7FFFFFFF) return PKV_ERR_INVALID;
+    auto s = static_cast<cudaStream_t>(stream);
+    const auto* ks = static_cast<const uint16_t*>(k_src);
+    const auto* vs = static_cast<const uint16_t*>(v_src);
+    auto* kp = static_cast<int8_t*>(c->k_pool);
+    auto* vp = static_cast<int8_t*>(c->v_pool);
+    if (c->head_dim == 128)
+        quantize_kernel<128><<<unsigned(grid), 128, 0, s>>>(ks, vs, from_tail, block_ids, slots, M, c->num_kv_heads,
+                                                            c->block_size, c->num_blocks, c->max_slots, kp, vp,
+                                                            c->scales, c->err_word);
+    else
+        quantize_kernel<64><<<unsigned(grid), 128, 0, s>>>(ks, vs, from_tail, block_ids, slots, M, c->num_kv_heads,
+                                                           c->block_size, c->num_blocks, c->max_slots, kp, vp,
+                                                           c->scales, c->err_word);
+    return cuda_status(cudaGetLastError());
+}
+
+int pkv_quantize_full_blocks(const pkv_cache_desc* c, const int32_t* block_ids, const int32_t* slots,
+                             int32_t M, void* stream) {
+    if (!c) return PKV_ERR_INVALID;
+    return quantize_common(c, c->k_tail, c->v_tail, 1, block_ids, slots, M, stream);
+}
+
+int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const void* v_src,
+                             const int32_t* block_ids, int32_t M, void* stream) {
+    return quantize_common(c, k_src, v_src, 0, block_ids, nullptr, M, stream);
+}
+
+static int launch_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_lens, int32_t B, int32_t Hq,
+                         int32_t head_dim, int32_t split_tokens, int32_t max_splits, void* out, int32_t* err,
+                         void* stream) {
+    if (B < 0 || Hq <= 0 || split_tokens <= 0 || max_splits <= 0) return PKV_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (B == 0) return PKV_OK;
+    if (!ws_o || !ws_ml || !ctx_lens || !out || B > 65535) return PKV_ERR_INVALID;
+    const size_t smem = size_t(max_splits) * sizeof(float);
+    if (smem > 48 * 1024) return PKV_ERR_UNSUPPORTED;
+    auto s = static_cast<cudaStream_t>(stream);
+    const dim3 grid{unsigned(Hq), unsigned(B), 1u};
+    auto* o = static_cast<uint16_t*>(out);
+    if (head_dim == 128)
+        splitk_reduce_kernel<128><<<grid, 128, smem, s>>>(ws_o, ws_ml, ctx_lens, Hq, split_tokens, max_splits, o,
+                                                          err);
+    else
+        splitk_reduce_kernel<64><<<grid, 128, smem, s>>>(ws_o, ws_ml, ctx_lens, Hq, split_tokens, max_splits, o,
+                                                         err);
+    return cuda_status(cudaGetLastError());
+}
+
+int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_lens, int32_t B, int32_t Hq,
+                      int32_t head_dim, int32_t split_tokens, int32_t max_splits, void* out, void* stream) {
+    return launch_reduce(ws_o, ws_ml, ctx_lens, B, Hq, head_dim, split_tokens, max_splits, out, nullptr, stream);
+}
+
+int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
+                         int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, void* out,
+                         void* stream) {
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (B < 0 || max_blocks <= 0 || split_tokens < 0 || !(sm_scale == sm_scale)) return PKV_ERR_INVALID;
+    if (B == 0) return PKV_OK;
+    if (!q || !block_tables || !ctx_lens || !out || B > 65535 || c->num_kv_heads > 65535) return PKV_ERR_INVALID;
+    if (!aligned16(q) || (reinterpret_cast<uintptr_t>(out) & 3u)) return PKV_ERR_INVALID;
+    const bool int8 = c->dtype == PKV_DTYPE_INT8;
+    if (int8 && !slots) return PKV_ERR_INVALID;
+    const int64_t max_ctx = int64_t(max_blocks) * c->block_size;
+    if (max_ctx > 0x7FFFFFFF) return PKV_ERR_INVALID;
+    const bool split = split_tokens > 0;
+    if (split) {
+        if (split_tokens % c->block_size || split_tokens % kTile) return PKV_ERR_INVALID;
+        if (int64_t(max_splits) * split_tokens < max_ctx || max_splits > 65535) return PKV_ERR_INVALID;
+        if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
+    }
+    const int g = c->num_q_heads / c->num_kv_heads;
+    int tab_cap = split ? split_tokens / c->block_size : max_blocks;
+    tab_cap += tab_cap & 1;
+    const size_t smem = decode_smem(c->head_dim, g, int8, tab_cap);
+    if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
+
+    DecodeParams p;
+    p.k_pool = c->k_pool;
+    p.v_pool = c->v_pool;
+    p.scales = c->scales;
+    p.k_tail = c->k_tail;
+    p.v_tail = c->v_tail;
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_tables = block_tables;
+    p.ctx_lens = ctx_lens;
+    p.slots = slots;
+    p.out = static_cast<uint16_t*>(out);
+    p.ws_o = ws_o;
+    p.ws_ml = ws_ml;
+    p.err = c->err_word;
+    p.Hq = c->num_q_heads;
+    p.Hkv = c->num_kv_heads;
+    p.bs = c->block_size;
+    p.max_blocks = max_blocks;
+    p.num_blocks = c->num_blocks;
+    p.max_slots = c->max_slots;
+    p.split_tokens = split_tokens;
+    p.max_splits = split ? max_splits : 1;
+    p.tab_cap = tab_cap;
+    p.qscale = sm_scale * 1.4426950408889634f;
+
+    const dim3 grid(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
+    auto s = static_cast<cudaStream_t>(stream);
+    int rc;
+    if (c->head_dim == 128) {
+        if (int8) rc = split ? dispatch_g<128, true, true>(g, p, grid, smem, s) : dispatch_g<128, true, false>(g, p, grid, smem, s);
+        else rc = split ? dispatch_g<128, false, true>(g, p, grid, smem, s) : dispatch_g<128, false, false>(g, p, grid, smem, s);
+    } else {
+        if (int8) rc = split ? dispatch_g<64, true, true>(g, p, grid, smem, s) : dispatch_g<64, true, false>(g, p, grid, smem, s);
+        else rc = split ? dispatch_g<64, false, true>(g, p, grid, smem, s) : dispatch_g<64, false, false>(g, p, grid, smem, s);
+    }
+    if (rc != PKV_OK || !split) return rc;
+    return launch_reduce(ws_o, ws_ml, ctx_lens, B, c->num_q_heads, c->head_dim, split_tokens, max_splits, out,
+                         c->err_word, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,311 @@
+"""Host-side runtime around the C ABI: per-layer device buffers, the block
+allocator, sequence slots, and the per-step control arrays (positions, block
+tables, context lengths, fill lists).
+
+Every computation on cache data runs in libpkv.so's kernels; this module only
+allocates device memory with torch, keeps host bookkeeping, and calls the
+binding. A decode step for B running sequences is:
+
+  1. (host) a sequence at position p with p % block_size == 0 gets a new
+     block from the allocator ([D] "连续批处理与KV缓存" §4.2 append_block);
+  2. (host -> device) block tables, context lengths, offsets and fill lists;
+  3. per layer: append the new K/V rows, quantize the blocks that filled
+     (INT8), decode attention (+ split-K merge).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import pkv
+
+
+class LayerCache:
+    """Device buffers of one layer and the descriptor that points at them."""
+
+    def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 block_size: int, int8: bool, max_slots: int, device="cuda"):
+        self.num_blocks, self.hq, self.hkv, self.d, self.bs = num_blocks, num_q_heads, num_kv_heads, head_dim, block_size
+        self.int8 = int8
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        pool_dtype = torch.int8 if int8 else torch.bfloat16
+        self.k_pool = torch.empty(shape, dtype=pool_dtype, device=device)
+        self.v_pool = torch.empty(shape, dtype=pool_dtype, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if int8:
+            self.scales = torch.zeros((num_blocks, num_kv_heads, 2), dtype=torch.float32, device=device)
+            tail_shape = (max_slots, num_kv_heads, block_size, head_dim)
+            self.k_tail = torch.zeros(tail_shape, dtype=torch.bfloat16, device=device)
+            self.v_tail = torch.zeros(tail_shape, dtype=torch.bfloat16, device=device)
+        else:
+            self.scales = self.k_tail = self.v_tail = None
+        self.desc = pkv.CacheDesc(
+            k_pool=self.k_pool.data_ptr(), v_pool=self.v_pool.data_ptr(),
+            scales=self.scales.data_ptr() if int8 else None,
+            k_tail=self.k_tail.data_ptr() if int8 else None,
+            v_tail=self.v_tail.data_ptr() if int8 else None,
+            num_blocks=num_blocks, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+            head_dim=head_dim, block_size=block_size, max_slots=max_slots if int8 else 0,
+            dtype=pkv.PKV_DTYPE_INT8 if int8 else pkv.PKV_DTYPE_BF16,
+            err_word=self.err.data_ptr())
+
+    def error_bits(self) -> int:
+        return int(self.err.item())
+
+
+def choose_split_tokens(batch: int, num_kv_heads: int, max_ctx: int, block_size: int,
+                        num_sms: int, ctas_per_sm: int = 3) -> int:
+    """Split length (a multiple of 16 and of block_size) that gives about
+    num_sms * ctas_per_sm CTAs for the longest context, or 0 when one CTA per
+    (sequence, kv head) already fills the GPU."""
+    pairs = batch * num_kv_heads
+    target = num_sms * ctas_per_sm
+    if pairs >= target or max_ctx <= 0:
+        return 0
+    splits = max(1, -(-target // pairs))
+    unit = max(16, block_size)
+    tok = -(-max_ctx // splits)
+    tok = -(-tok // unit) * unit
+    return max(unit, tok)
+
+
+@dataclass
+class Seq:
+    req_id: int
+    slot: int
+    length: int = 0  # tokens already in the cache
+
+
+@dataclass
+class StepPlan:
+    """Host arrays describing one decode step of B sequences."""
+    positions: np.ndarray      # [B] token index written this step
+    ctx_lens: np.ndarray       # [B] tokens attended over (positions + 1)
+    offsets: np.ndarray        # [B] positions % block_size
+    block_ids: np.ndarray      # [B] block receiving the new row
+    slots: np.ndarray          # [B]
+    fill_blocks: np.ndarray    # [B] block that filled this step, or -1
+    tables: np.ndarray         # [B, max_blocks]
+    tables_changed: bool = True
+
+
+class PagedKVCache:
+    """L layers of paged cache sharing one allocator and one slot space."""
+
+    def __init__(self, num_layers: int, num_blocks: int, num_q_heads: int, num_kv_heads: int,
+                 head_dim: int, block_size: int, int8: bool, max_slots: int, max_blocks_per_seq: int,
+                 device="cuda", initial_order=None):
+        self.L = num_layers
+        self.bs = block_size
+        self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
+        self.int8 = int8
+        self.max_slots = max_slots
+        self.max_blocks = max_blocks_per_seq
+        self.device = device
+        self.layers = [LayerCache(num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, int8,
+                                  max_slots, device) for _ in range(num_layers)]
+        self.alloc = pkv.pkv_allocator_create(num_blocks, block_size, initial_order)
+        self.free_slots = list(range(max_slots))
+        self.seqs: dict[int, Seq] = {}
+
+    def close(self):
+        if self.alloc is not None:
+            pkv.pkv_allocator_destroy(self.alloc)
+            self.alloc = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- requests ------------------------------------------------------------
+    def add_sequence(self, req_id: int, n_blocks: int = 0, shared_blocks=()) -> Seq:
+        if not self.free_slots:
+            raise RuntimeError("no free sequence slot")
+        pkv.pkv_alloc(self.alloc, req_id, n_blocks)
+        if len(shared_blocks):
+            pkv.pkv_attach_shared(self.alloc, req_id, list(shared_blocks))
+        s = Seq(req_id, self.free_slots.pop(0), 0)
+        self.seqs[req_id] = s
+        return s
+
+    def remove_sequence(self, req_id: int) -> None:
+        s = self.seqs.pop(req_id)
+        pkv.pkv_free(self.alloc, req_id)
+        self.free_slots.append(s.slot)
+
+    def table(self, req_id: int) -> list:
+        return pkv.pkv_request_table(self.alloc, req_id)
+
+    # -- one decode step -----------------------------------------------------
+    def plan_step(self, req_ids, tables_out: np.ndarray | None = None) -> StepPlan:
+        """Host part of one decode step: grows block lists where a new block
+        starts, and builds the control arrays. Raises PkvError(OOM) if a
+        needed block is not available (the caller decides whether to wait)."""
+        B = len(req_ids)
+        pos = np.empty(B, np.int32)
+        blk = np.empty(B, np.int32)
+        fill = np.full(B, -1, np.int32)
+        slots = np.empty(B, np.int32)
+        changed = False
+        for i, r in enumerate(req_ids):
+            s = self.seqs[r]
+            p = s.length
+            if p % self.bs == 0 and len(self.table(r)) <= p // self.bs:
+                pkv.pkv_append_block(self.alloc, r)
+                changed = True
+            pos[i] = p
+            slots[i] = s.slot
+        tables = pkv.pkv_build_block_tables(self.alloc, req_ids, self.max_blocks, tables_out)
+        for i, r in enumerate(req_ids):
+            p = int(pos[i])
+            blk[i] = tables[i, p // self.bs]
+            if self.int8 and (p + 1) % self.bs == 0:
+                fill[i] = blk[i]
+        return StepPlan(positions=pos, ctx_lens=pos + 1, offsets=pos % self.bs, block_ids=blk,
+                        slots=slots, fill_blocks=fill, tables=tables, tables_changed=changed)
+
+    def commit_step(self, req_ids) -> None:
+        for r in req_ids:
+            self.seqs[r].length += 1
+
+
+def sm_scale_for(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)
+
+
+# ---------------------------------------------------------------------------
+# Prefill (untimed setup: writes a prompt's rows with the same two kernels)
+# ---------------------------------------------------------------------------
+
+def prefill(cache: PagedKVCache, layer: int, req_ids, k_rows, v_rows, starts=None, stream=None) -> None:
+    """Writes rows k_rows[i] / v_rows[i] ([n_i, Hkv, d] bf16, device) of
+    sequence req_ids[i] at positions starts[i] .. starts[i]+n_i-1 (starts must
+    be multiples of block_size; the sequence must already hold the blocks).
+    BF16 cache: one append of all rows. INT8 cache: whole blocks are quantized
+    straight from the rows; the trailing partial block goes to the tail."""
+    lc = cache.layers[layer]
+    bs = cache.bs
+    dev = lc.k_pool.device
+    starts = [0] * len(req_ids) if starts is None else list(starts)
+    tabs = [cache.table(r) for r in req_ids]
+    if not cache.int8:
+        blk, off = [], []
+        for t, s0, k in zip(tabs, starts, k_rows):
+            pos = np.arange(s0, s0 + k.shape[0])
+            blk.append(np.asarray(t, np.int32)[pos // bs])
+            off.append((pos % bs).astype(np.int32))
+        if sum(k.shape[0] for k in k_rows) == 0:
+            return
+        pkv.pkv_append_kv(lc.desc, torch.cat(list(k_rows)).contiguous(), torch.cat(list(v_rows)).contiguous(),
+                          torch.from_numpy(np.concatenate(blk)).to(dev), torch.from_numpy(np.concatenate(off)).to(dev),
+                          None, stream)
+        return
+    fk, fv, fb, tk, tv, ts, to = [], [], [], [], [], [], []
+    for r, t, s0, k, v in zip(req_ids, tabs, starts, k_rows, v_rows):
+        if s0 % bs:
+            raise ValueError("prefill start must be a multiple of block_size")
+        n = k.shape[0]
+        nf = n // bs
+        if nf:
+            fk.append(k[: nf * bs])
+            fv.append(v[: nf * bs])
+            fb.extend(t[s0 // bs: s0 // bs + nf])
+        if n % bs:
+            tk.append(k[nf * bs:])
+            tv.append(v[nf * bs:])
+            ts.extend([cache.seqs[r].slot] * (n % bs))
+            to.extend(range(n % bs))
+    if fb:
+        pkv.pkv_quantize_blocks_from(lc.desc, torch.cat(fk).contiguous(), torch.cat(fv).contiguous(),
+                                     torch.tensor(fb, dtype=torch.int32, device=dev), stream)
+    if ts:
+        pkv.pkv_append_kv(lc.desc, torch.cat(tk).contiguous(), torch.cat(tv).contiguous(), None,
+                          torch.tensor(to, dtype=torch.int32, device=dev),
+                          torch.tensor(ts, dtype=torch.int32, device=dev), stream)
+
+
+# ---------------------------------------------------------------------------
+# Decode steps
+# ---------------------------------------------------------------------------
+
+class StepBuffers:
+    """Device-side control arrays (and split-K workspace) of decode steps for
+    up to max_batch sequences; pinned host mirrors make the uploads async."""
+
+    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int = 0):
+        dev = cache.device
+        self.cache = cache
+        self.max_batch = max_batch
+        self.split_tokens = split_tokens
+        mb = cache.max_blocks
+        self.max_splits = -(-(mb * cache.bs) // split_tokens) if split_tokens else 0
+
+        def pair(shape):
+            return (torch.zeros(shape, dtype=torch.int32).pin_memory(),
+                    torch.zeros(shape, dtype=torch.int32, device=dev))
+        self.h_ctx, self.ctx = pair(max_batch)
+        self.h_off, self.off = pair(max_batch)
+        self.h_blk, self.blk = pair(max_batch)
+        self.h_slot, self.slot = pair(max_batch)
+        self.h_fill, self.fill = pair(max_batch)
+        self.h_tab, self.tab = pair((max_batch, mb))
+        if split_tokens:
+            self.ws_o = torch.empty(max_batch * cache.hq * self.max_splits * cache.d, dtype=torch.float32, device=dev)
+            self.ws_ml = torch.empty(max_batch * cache.hq * self.max_splits * 2, dtype=torch.float32, device=dev)
+        else:
+            self.ws_o = self.ws_ml = None
+        self.B = 0
+        self.copied = torch.cuda.Event()  # the last upload's copies have run
+        self.copied.record()
+
+    def upload(self, plan: StepPlan) -> None:
+        B = len(plan.positions)
+        if B > self.max_batch:
+            raise ValueError("batch larger than the step buffers")
+        self.B = B
+        self.copied.synchronize()  # do not overwrite pinned data a pending copy still reads
+        self.h_ctx[:B].numpy()[:] = plan.ctx_lens
+        self.h_off[:B].numpy()[:] = plan.offsets
+        self.h_blk[:B].numpy()[:] = plan.block_ids
+        self.h_slot[:B].numpy()[:] = plan.slots
+        self.h_fill[:B].numpy()[:] = plan.fill_blocks
+        for h, d in ((self.h_ctx, self.ctx), (self.h_off, self.off), (self.h_blk, self.blk),
+                     (self.h_slot, self.slot), (self.h_fill, self.fill)):
+            d[:B].copy_(h[:B], non_blocking=True)
+        self.h_tab[:B].numpy()[:] = plan.tables
+        self.tab[:B].copy_(self.h_tab[:B], non_blocking=True)
+        self.copied.record()
+
+
+def run_layers(cache: PagedKVCache, bufs: StepBuffers, q, k_new, v_new, out, sm_scale: float,
+               quantize: str = "auto", plan: StepPlan | None = None, stream=None) -> None:
+    """Kernel launches of one decode step for bufs.B sequences: per layer l,
+    append k_new[l], v_new[l] ([B, Hkv, d]), quantize filled blocks (INT8),
+    attend with q[l] ([B, Hq, d]) into out[l] ([B, Hq, d]).
+
+    quantize="auto" launches the quantize kernel only when the plan has a
+    filled block; "always" launches it every step over a -1-padded list (the
+    form a captured CUDA graph needs)."""
+    B = bufs.B
+    for li, lc in enumerate(cache.layers):
+        pkv.pkv_append_kv(lc.desc, k_new[li], v_new[li], bufs.blk[:B], bufs.off[:B], bufs.slot[:B], stream)
+        if cache.int8 and (quantize == "always" or (plan is not None and (plan.fill_blocks >= 0).any())):
+            pkv.pkv_quantize_full_blocks(lc.desc, bufs.fill[:B], bufs.slot[:B], stream)
+        pkv.pkv_decode_attention(lc.desc, q[li], bufs.tab[:B], bufs.ctx[:B], bufs.slot[:B], sm_scale, out[li],
+                                 bufs.split_tokens, bufs.max_splits, bufs.ws_o, bufs.ws_ml, stream)
+
+
+def decode_step(cache: PagedKVCache, bufs: StepBuffers, req_ids, q, k_new, v_new, out, sm_scale: float,
+                stream=None) -> StepPlan:
+    """Host plan + upload + kernels of one decode step; advances the sequences."""
+    plan = cache.plan_step(req_ids)
+    bufs.upload(plan)
+    run_layers(cache, bufs, q, k_new, v_new, out, sm_scale, "auto", plan, stream)
+    cache.commit_step(req_ids)
+    return plan

@@ -1,0 +1,154 @@
+"""Test harness: one seeded workload driven through the C ABI (GPU) and,
+independently, through the oracle (CPU), from the same counter-based inputs.
+
+Nothing here computes cache arithmetic: the GPU side calls libpkv.so through
+the runtime, the CPU side calls ``oracle``. Both read their inputs from
+``paged_kv_cache_56_gb300.synth``, which regenerates any row on any device.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from oracle.attention import decode_attention
+from oracle.cache import SequenceHistory
+from paged_kv_cache_56_gb300 import synth
+from paged_kv_cache_56_gb300.runtime import PagedKVCache, StepBuffers, decode_step, prefill
+
+ATOL, RTOL = 2e-3, 1e-2  # |gpu - ref| <= ATOL + RTOL * |ref| on bf16 outputs
+
+
+def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> None:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bad = np.abs(gpu - ref) > ATOL + RTOL * np.abs(ref)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first at {tuple(i)}: "
+                             f"gpu {gpu[tuple(i)]!r} ref {ref[tuple(i)]!r}; max err "
+                             f"{np.max(np.abs(gpu - ref)):.3g}")
+
+
+class Workload:
+    """L layers, B sequences with prior lengths ``prior``; decode steps t = 0, 1, ..."""
+
+    def __init__(self, seed: int, num_layers: int, prior, Hq: int, Hkv: int, d: int, bs: int,
+                 num_blocks: int, int8: bool, split_tokens: int = 0, max_blocks: int | None = None,
+                 head_scale: bool = False, outliers: bool = False, shuffle: bool = True,
+                 req_ids=None, device="cuda", layers_with_data=None):
+        self.seed, self.L, self.prior = seed, num_layers, list(prior)
+        self.Hq, self.Hkv, self.d, self.bs = Hq, Hkv, d, bs
+        self.int8 = int8
+        self.head_scale, self.outliers = head_scale, outliers
+        self.B = len(self.prior)
+        self.req_ids = list(req_ids) if req_ids is not None else list(range(100, 100 + self.B))
+        self.sm_scale = 1.0 / math.sqrt(d)
+        self.device = device
+        self.max_blocks = max_blocks or -(-(max(self.prior) + 64) // bs)
+        order = synth.permutation(seed, num_blocks) if shuffle else None
+        self.cache = PagedKVCache(num_layers, num_blocks, Hq, Hkv, d, bs, int8, max_slots=self.B,
+                                  max_blocks_per_seq=self.max_blocks, device=device, initial_order=order)
+        self.bufs = StepBuffers(self.cache, self.B, split_tokens)
+        self.step_no = 0
+        for r, n in zip(self.req_ids, self.prior):
+            self.cache.add_sequence(r, -(-n // bs))
+        for li in range(num_layers):
+            ks = [self.kv(li, synth.KIND_K, r, torch.arange(n)) for r, n in zip(self.req_ids, self.prior)]
+            vs = [self.kv(li, synth.KIND_V, r, torch.arange(n)) for r, n in zip(self.req_ids, self.prior)]
+            prefill(self.cache, li, self.req_ids, ks, vs)
+        for r, n in zip(self.req_ids, self.prior):
+            self.cache.seqs[r].length = n
+        torch.cuda.synchronize()
+
+    # -- inputs (shared generator) ------------------------------------------
+    def kv_mult(self, layer, kind):
+        if self.outliers:
+            return synth.outlier_multipliers(self.seed, layer, kind, self.Hkv, self.d)
+        if self.head_scale:
+            return synth.head_multipliers(self.seed, layer, kind, self.Hkv)
+        return None
+
+    def q_mult(self, layer):
+        return synth.head_multipliers(self.seed, layer, synth.KIND_Q, self.Hq) if self.head_scale else None
+
+    def kv(self, layer, kind, req, positions, device=None):
+        return synth.kv_rows(self.seed, layer, kind, req, positions, self.Hkv, self.d,
+                             mult=self.kv_mult(layer, kind), device=device or self.device)
+
+    def q(self, layer, step, reqs, device=None):
+        return synth.q_rows(self.seed, layer, step, reqs, self.Hq, self.d, mult=self.q_mult(layer),
+                            device=device or self.device)
+
+    # -- GPU ------------------------------------------------------------------
+    def step(self):
+        """One decode step through the C ABI; returns out [L, B, Hq, d] (device bf16)."""
+        t = self.step_no
+        lens = [self.cache.seqs[r].length for r in self.req_ids]
+        pos = torch.tensor(lens, dtype=torch.int64)
+        q = [self.q(li, t, self.req_ids) for li in range(self.L)]
+        kn = [self.kv(li, synth.KIND_K, self.req_ids, pos) for li in range(self.L)]
+        vn = [self.kv(li, synth.KIND_V, self.req_ids, pos) for li in range(self.L)]
+        out = torch.empty((self.L, self.B, self.Hq, self.d), dtype=torch.bfloat16, device=self.device)
+        decode_step(self.cache, self.bufs, self.req_ids, q, kn, vn, list(out), self.sm_scale)
+        self.step_no += 1
+        return out
+
+    def error_bits(self) -> int:
+        return sum(lc.error_bits() for lc in self.cache.layers)
+
+    # -- oracle ---------------------------------------------------------------
+    def history(self, layer: int, i: int, n: int) -> SequenceHistory:
+        r = self.req_ids[i]
+        h = SequenceHistory(self.Hkv, self.d, self.bs, self.int8)
+        pos = torch.arange(n)
+        h.append(self.kv(layer, synth.KIND_K, r, pos, "cpu").float().numpy(),
+                 self.kv(layer, synth.KIND_V, r, pos, "cpu").float().numpy())
+        return h
+
+    def oracle_out(self, layer: int, i: int, step: int, heads=None) -> np.ndarray:
+        """Oracle output [Hq, d] of sequence i at decode step ``step``."""
+        n = self.prior[i] + step + 1
+        h = self.history(layer, i, n)
+        k, v = h.context()
+        q = self.q(layer, step, [self.req_ids[i]], "cpu")[0].float().numpy()
+        return decode_attention(q, k, v, self.sm_scale)
+
+    def check_pool_bytes(self, layer: int, i: int, n: int) -> int:
+        """Compares the pools of sequence i (first n tokens) with the oracle's
+        history byte for byte; returns the number of blocks compared."""
+        h = self.history(layer, i, n)
+        lc = self.cache.layers[layer]
+        tab = self.cache.table(self.req_ids[i])
+        nf = n // self.bs
+        if self.int8:
+            kp = lc.k_pool.cpu().numpy()
+            vp = lc.v_pool.cpu().numpy()
+            sc = lc.scales.cpu().numpy()
+            for bi in range(nf):
+                qk, sk, qv, sv = h.blocks[bi]
+                pb = tab[bi]
+                assert np.array_equal(kp[pb], qk), (layer, i, bi, "K codes")
+                assert np.array_equal(vp[pb], qv), (layer, i, bi, "V codes")
+                assert np.array_equal(sc[pb, :, 0].view(np.uint32), sk.view(np.uint32)), (layer, i, bi, "K scale")
+                assert np.array_equal(sc[pb, :, 1].view(np.uint32), sv.view(np.uint32)), (layer, i, bi, "V scale")
+            rem = n - nf * self.bs
+            if rem:
+                slot = self.cache.seqs[self.req_ids[i]].slot
+                kr, vr = h.raw()
+                kt = lc.k_tail[slot, :, :rem].float().cpu().numpy()
+                assert np.array_equal(kt, kr[nf * self.bs:].transpose(1, 0, 2)), (layer, i, "K tail")
+                vt = lc.v_tail[slot, :, :rem].float().cpu().numpy()
+                assert np.array_equal(vt, vr[nf * self.bs:].transpose(1, 0, 2)), (layer, i, "V tail")
+            return nf
+        kp = lc.k_pool.float().cpu().numpy()
+        vp = lc.v_pool.float().cpu().numpy()
+        kr, vr = h.raw()
+        for bi in range(-(-n // self.bs)):
+            lo, hi = bi * self.bs, min(n, (bi + 1) * self.bs)
+            pb = tab[bi]
+            assert np.array_equal(kp[pb][:, : hi - lo], kr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "K rows")
+            assert np.array_equal(vp[pb][:, : hi - lo], vr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "V rows")
+        return -(-n // self.bs)

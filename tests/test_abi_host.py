@@ -1,0 +1,193 @@
+"""The C ABI on the host: exported symbols, argument validation that returns
+before any CUDA call, and the C++ allocator against the oracle allocator."""
+
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from libpkv import ensure_built
+from oracle.allocator import FreeBlockPool, OutOfBlocks, UnknownRequest, DuplicateRequest
+from paged_kv_cache_56_gb300 import pkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    return ensure_built()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(pkv.EXPORTED) == names
+
+
+def test_desc_layout_matches_header():
+    # 5 pointers, 7 int32, 1 pointer (with padding before it)
+    assert ctypes.sizeof(pkv.CacheDesc) == 5 * 8 + 7 * 4 + 4 + 8
+
+
+def _desc(**kw):
+    d = dict(k_pool=16, v_pool=32, scales=None, k_tail=None, v_tail=None, num_blocks=4, num_q_heads=4,
+             num_kv_heads=2, head_dim=128, block_size=16, max_slots=0, dtype=pkv.PKV_DTYPE_BF16, err_word=None)
+    d.update(kw)
+    return pkv.CacheDesc(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(block_size=32), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(num_q_heads=6, num_kv_heads=4), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(num_q_heads=16, num_kv_heads=2), pkv.PKV_ERR_UNSUPPORTED),   # G = 8 at d = 128
+    (dict(k_pool=None), pkv.PKV_ERR_INVALID),
+    (dict(k_pool=24), pkv.PKV_ERR_INVALID),                           # misaligned pool
+    (dict(dtype=7), pkv.PKV_ERR_INVALID),
+    (dict(dtype=pkv.PKV_DTYPE_INT8), pkv.PKV_ERR_INVALID),            # INT8 without tails/scales
+])
+def test_descriptor_validation(L, kw, code):
+    d = _desc(**kw)
+    rc = L.pkv_decode_attention(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None)
+    assert rc == code
+    rc = L.pkv_append_kv(ctypes.byref(d), 16, 16, 16, 16, 16, 1, None)
+    assert rc == code
+
+
+def test_argument_validation(L):
+    d = _desc()
+    attn = L.pkv_decode_attention
+    assert attn(None, 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 0, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_OK  # B = 0
+    assert attn(ctypes.byref(d), None, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 0, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, float("nan"), 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    # split must be a multiple of block size and of 16; max_splits must cover max_blocks * bs
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 24, 8, 16, 16, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 1, 16, 16, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 2, None, 16, 16, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_append_kv(ctypes.byref(d), 16, 16, 16, 16, 16, 0, None) == pkv.PKV_OK  # T = 0
+    assert L.pkv_append_kv(ctypes.byref(d), 16, 16, None, 16, 16, 3, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_quantize_full_blocks(ctypes.byref(d), 16, 16, 1, None) == pkv.PKV_ERR_INVALID  # BF16 cache
+    assert L.pkv_splitk_reduce(16, 16, 16, 1, 4, 96, 16, 2, 16, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert L.pkv_splitk_reduce(16, 16, 16, 1, 4, 128, 0, 2, 16, None) == pkv.PKV_ERR_INVALID
+    assert pkv.pkv_splitk_ws_o_bytes(2, 3, 128, 5) == 2 * 3 * 5 * 128 * 4
+    assert pkv.pkv_splitk_ws_ml_bytes(2, 3, 5) == 2 * 3 * 5 * 2 * 4
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    d = _desc()
+    with pytest.raises(ValueError):
+        pkv.pkv_decode_attention(d, torch.zeros(4, 128, dtype=torch.bfloat16), torch.zeros(1, 4, dtype=torch.int32),
+                                 torch.ones(1, dtype=torch.int32), None, 0.1,
+                                 torch.zeros(4, 128, dtype=torch.bfloat16))
+
+
+# -- allocator -----------------------------------------------------------------
+
+def test_allocator_replays_oracle_ids(L):
+    rng = random.Random(1234)
+    n = 97
+    order = rng.sample(range(n), n)
+    h = pkv.pkv_allocator_create(n, 16, order)
+    ref = FreeBlockPool(n, order)
+    live = []
+    try:
+        for i in range(100_000):
+            u = rng.random()
+            if u < 0.3:
+                k = rng.randint(0, 9)
+                try:
+                    want = ref.alloc(i, k)
+                except OutOfBlocks:
+                    with pytest.raises(pkv.PkvError) as e:
+                        pkv.pkv_alloc(h, i, k)
+                    assert e.value.code == pkv.PKV_ERR_OOM
+                else:
+                    assert pkv.pkv_alloc(h, i, k) == want
+                    live.append(i)
+            elif u < 0.75 and live:
+                r = rng.choice(live)
+                want = ref.append_block(r)
+                if want is None:
+                    with pytest.raises(pkv.PkvError) as e:
+                        pkv.pkv_append_block(h, r)
+                    assert e.value.code == pkv.PKV_ERR_OOM
+                else:
+                    assert pkv.pkv_append_block(h, r) == want
+            elif live:
+                r = live.pop(rng.randrange(len(live)))
+                ref.free(r)
+                pkv.pkv_free(h, r)
+            if i % 997 == 0:
+                assert pkv.pkv_free_list(h) == ref.free_list
+                for r in live[:5]:
+                    assert pkv.pkv_request_table(h, r) == ref.table(r)
+        assert pkv.pkv_num_free(h) == ref.num_free()
+        assert pkv.pkv_free_list(h) == ref.free_list
+    finally:
+        pkv.pkv_allocator_destroy(h)
+
+
+def test_allocator_errors_and_shared_blocks(L):
+    h = pkv.pkv_allocator_create(10, 16)
+    ref = FreeBlockPool(10)
+    try:
+        prefix = pkv.pkv_alloc(h, -1, 3)
+        assert prefix == ref.alloc(-1, 3)
+        for r in (5, 6):
+            assert pkv.pkv_alloc(h, r, 1) == ref.alloc(r, 1)
+            pkv.pkv_attach_shared(h, r, prefix)
+            ref.attach_shared(r, prefix)
+        assert pkv.pkv_request_table(h, 5) == ref.table(5) == prefix + [3]
+        for fn, args, code in [(pkv.pkv_alloc, (5, 1), pkv.PKV_ERR_EXISTS),
+                               (pkv.pkv_free, (77,), pkv.PKV_ERR_NOT_FOUND),
+                               (pkv.pkv_append_block, (77,), pkv.PKV_ERR_NOT_FOUND),
+                               (pkv.pkv_alloc, (8, 6), pkv.PKV_ERR_OOM),
+                               (pkv.pkv_attach_shared, (5, [10]), pkv.PKV_ERR_INVALID)]:
+            with pytest.raises(pkv.PkvError) as e:
+                fn(h, *args)
+            assert e.value.code == code
+        assert pkv.pkv_free_list(h) == ref.free_list
+        pkv.pkv_free(h, 5)
+        ref.free(5)
+        assert pkv.pkv_free_list(h) == ref.free_list == [5, 6, 7, 8, 9, 3]
+        tab = pkv.pkv_build_block_tables(h, [6, -1], 5)
+        assert tab.tolist() == [prefix + [4, -1], prefix + [-1, -1]]
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_build_block_tables(h, [6], 3)
+        assert e.value.code == pkv.PKV_ERR_INVALID
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_build_block_tables(h, [5], 8)
+        assert e.value.code == pkv.PKV_ERR_NOT_FOUND
+    finally:
+        pkv.pkv_allocator_destroy(h)
+
+
+def test_allocator_create_rejects_bad_order(L):
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_allocator_create(4, 16, [0, 1, 1, 2])
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_allocator_create(0, 16)
+
+
+def test_page_sizing_through_the_allocator(L):
+    # A 600-token sequence in 16-token blocks holds 38 blocks (tail waste 8 < 16).
+    h = pkv.pkv_allocator_create(2048, 16)
+    try:
+        ids = pkv.pkv_alloc(h, 1, -(-600 // 16))
+        assert len(ids) == 38 and pkv.pkv_num_free(h) == 2010
+    finally:
+        pkv.pkv_allocator_destroy(h)

@@ -1,0 +1,55 @@
+"""GPU parity on the tiny configuration (1 layer, 4 sequences, Hq=4, Hkv=2,
+d=64, block 16, 64-block pool, seeded shuffled pool), bf16 and INT8 caches,
+every split setting, element by element against the oracle; plus the
+quantizer's bytes and scales, bit for bit."""
+
+import numpy as np
+import pytest
+import torch
+
+from harness import Workload, assert_close
+from libpkv import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+TINY = dict(num_layers=1, Hq=4, Hkv=2, d=64, bs=16, num_blocks=64)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+@pytest.mark.parametrize("split", [0, 16, 32, 64])
+@pytest.mark.parametrize("prior", [(1, 17, 33, 100), (15, 16, 31, 0)])
+def test_tiny_decode_steps(int8, split, prior):
+    w = Workload(seed=1234, prior=prior, int8=int8, split_tokens=split, max_blocks=9, **TINY)
+    for t in range(18):  # crosses a block boundary for every sequence
+        out = w.step().float().cpu().numpy()
+        for i in range(w.B):
+            assert_close(out[0, i], w.oracle_out(0, i, t), f"step {t} seq {i}")
+    assert w.error_bits() == 0
+    for i in range(w.B):
+        w.check_pool_bytes(0, i, prior[i] + 18)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_block_permutation_is_bit_identical(int8):
+    outs = []
+    for shuffle in (False, True):
+        w = Workload(seed=77, prior=(40, 100, 7, 64), int8=int8, shuffle=shuffle, split_tokens=32, max_blocks=9,
+                     **TINY)
+        outs.append(torch.stack([w.step() for _ in range(3)]).cpu())
+    assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_split_counts_agree(int8):
+    res = {}
+    for split in (0, 16, 48, 112):
+        w = Workload(seed=5, prior=(100, 3, 77, 111), int8=int8, split_tokens=split, max_blocks=8, **TINY)
+        res[split] = w.step().float().cpu().numpy()
+    for split in (16, 48, 112):
+        assert_close(res[split], res[0], f"split {split} vs none")
