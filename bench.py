@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the paged KV cache on GB300.
+
+A step is one decode step of every running sequence through all layers:
+host block allocation and tables, their upload, then per layer append +
+quantize-on-fill + decode attention (+ split-K merge). Inputs are seeded
+synthetic rows, generated on the device before timing; the KV working set of
+a step (1.84 GB for the default workload) is far larger than L2, so no flush
+is needed between steps.
+
+Default workload: GQA TTS-talker decode -- 28 layers, 4 sequences x 8000
+context tokens, Hq=16, Hkv=8, d=128, 16-token blocks, INT8 cache with a bf16
+tail, per-head scales U(0.1, 4). Other workloads: --workload mha7b | long_bf16
+| long_int8 | tiny.
+
+Metric: KV GB/s = algorithmic bytes the attention must read per step / step
+time, plus decode tokens/s. ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: layers, batch, prior tokens, Hq, Hkv, d, block, pool blocks/layer, int8, head scale, outliers, repeat
+    "tts_talker": dict(L=28, B=4, prior=8000, Hq=16, Hkv=8, d=128, bs=16, num_blocks=2048, int8=True,
+                       head_scale=True, outliers=False, repeat=1,
+                       desc="GQA TTS-talker decode: 28 layers, 4 x 8000 ctx, Hq=16 Hkv=8 d=128, bs=16, INT8"),
+    "mha7b": dict(L=32, B=100, prior=1024, Hq=32, Hkv=32, d=128, bs=16, num_blocks=8192, int8=False,
+                  head_scale=False, outliers=False, repeat=1,
+                  desc="MHA 7B-class decode: 32 layers, 100 x 1024 ctx, 32 heads d=128, bs=16, bf16"),
+    "long_bf16": dict(L=1, B=8, prior=32768, Hq=32, Hkv=8, d=128, bs=64, num_blocks=4200, int8=False,
+                      head_scale=False, outliers=True, repeat=32,
+                      desc="long-context split-K: 8 x 32768 ctx, Hq=32 Hkv=8 d=128, bs=64, bf16, 1 layer x32"),
+    "long_int8": dict(L=1, B=8, prior=32768, Hq=32, Hkv=8, d=128, bs=64, num_blocks=4200, int8=True,
+                      head_scale=False, outliers=True, repeat=32,
+                      desc="long-context split-K: 8 x 32768 ctx, Hq=32 Hkv=8 d=128, bs=64, INT8, 1 layer x32"),
+    "tiny": dict(L=1, B=4, prior=[1, 17, 33, 100], Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=True,
+                 head_scale=False, outliers=False, repeat=1,
+                 desc="tiny correctness case: 1 layer, ctx {1,17,33,100}, Hq=4 Hkv=2 d=64, bs=16"),
+}
+SEED = 1234
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic: what the method must read/write, nothing else)
+# ---------------------------------------------------------------------------
+
+def attention_bytes(ctx_lens, Hq, Hkv, d, bs, int8) -> int:
+    """Bytes one attention call must move: the KV of every attended token
+    (int8 full blocks at 1 B/elem plus one fp32 scale per block, head and
+    K|V; bf16 tail or bf16 cache at 2 B/elem), one int32 table entry per
+    block, q in and out (bf16)."""
+    total = 0
+    for n in ctx_lens:
+        n = int(n)
+        nblk = -(-n // bs)
+        if int8:
+            full = (n // bs) * bs
+            total += full * Hkv * 2 * d * 1 + (n - full) * Hkv * 2 * d * 2 + (n // bs) * Hkv * 2 * 4
+        else:
+            total += n * Hkv * 2 * d * 2
+        total += nblk * 4 + Hq * d * 2 * 2
+    return total
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        out["sm_mhz"] = statistics.median(float(r[1]) for r in rows)
+        out["sm_max_mhz"] = max(float(r[2]) for r in rows)
+        out["reasons"] = sorted(reasons)
+        out["samples"] = len(rows)
+        return out
+
+
+# ---------------------------------------------------------------------------
+# the device arm
+# ---------------------------------------------------------------------------
+
+class Bench:
+    def __init__(self, wl: dict, device: str, steps_total: int):
+        from paged_kv_cache_56_gb300 import synth
+        from paged_kv_cache_56_gb300.runtime import PagedKVCache, StepBuffers, choose_split_tokens, prefill
+
+        self.wl = wl
+        self.synth = synth
+        self.device = device
+        L, B, Hq, Hkv, d, bs = wl["L"], wl["B"], wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
+        prior = wl["prior"] if isinstance(wl["prior"], list) else [wl["prior"]] * B
+        self.prior = prior
+        self.reqs = list(range(1000, 1000 + B))
+        self.sm_scale = 1.0 / math.sqrt(d)
+        max_blocks = -(-(max(prior) + steps_total + 1) // bs)
+        self.cache = PagedKVCache(L, wl["num_blocks"], Hq, Hkv, d, bs, wl["int8"], max_slots=B,
+                                  max_blocks_per_seq=max_blocks, device=device,
+                                  initial_order=synth.permutation(SEED, wl["num_blocks"]))
+        props = torch.cuda.get_device_properties(torch.device(device))
+        self.split = choose_split_tokens(B, Hkv, max(prior) + steps_total + 1, bs, props.multi_processor_count)
+        self.bufs = StepBuffers(self.cache, B, self.split)
+        for r, n in zip(self.reqs, prior):
+            self.cache.add_sequence(r, -(-n // bs))
+        for li in range(L):
+            ks = [self.kv(li, synth.KIND_K, r, torch.arange(n, device=device)) for r, n in zip(self.reqs, prior)]
+            vs = [self.kv(li, synth.KIND_V, r, torch.arange(n, device=device)) for r, n in zip(self.reqs, prior)]
+            prefill(self.cache, li, self.reqs, ks, vs)
+            del ks, vs
+        for r, n in zip(self.reqs, prior):
+            self.cache.seqs[r].length = n
+        torch.cuda.synchronize()
+        self.R = wl["repeat"]
+        self.launches = 0
+
+    def kv_mult(self, layer, kind):
+        wl, s = self.wl, self.synth
+        if wl["outliers"]:
+            return s.outlier_multipliers(SEED, layer, kind, wl["Hkv"], wl["d"])
+        if wl["head_scale"]:
+            return s.head_multipliers(SEED, layer, kind, wl["Hkv"])
+        return None
+
+    def kv(self, layer, kind, req, pos):
+        wl = self.wl
+        return self.synth.kv_rows(SEED, layer, kind, req, pos, wl["Hkv"], wl["d"], mult=self.kv_mult(layer, kind),
+                                  device=self.device)
+
+    def step_inputs(self, step: int):
+        """Device tensors q [L*R, B, Hq, d], k/v [L, B, Hkv, d] for decode step ``step``."""
+        wl, s = self.wl, self.synth
+        pos = torch.tensor([n + step for n in self.prior], dtype=torch.int64, device=self.device)
+        qm = lambda li: s.head_multipliers(SEED, li, s.KIND_Q, wl["Hq"]) if wl["head_scale"] else None
+        q = torch.stack([s.q_rows(SEED, li, step, self.reqs, wl["Hq"], wl["d"], mult=qm(li), device=self.device)
+                         for li in range(wl["L"] * self.R)])
+        k = torch.stack([self.kv(li, s.KIND_K, self.reqs, pos) for li in range(wl["L"])])
+        v = torch.stack([self.kv(li, s.KIND_V, self.reqs, pos) for li in range(wl["L"])])
+        return q, k, v
+
+    def step(self, gs, q, k, v, graph: bool):
+        """One decode step: host plan + control uploads, this step's inputs
+        into the graph's static buffers, then the layer loop."""
+        plan = self.cache.plan_step(self.reqs)
+        self.bufs.upload(plan)
+        gs.q.copy_(q, non_blocking=True)
+        gs.k.copy_(k, non_blocking=True)
+        gs.v.copy_(v, non_blocking=True)
+        if graph:
+            gs.replay()
+        else:
+            gs.run_eager()
+        self.cache.commit_step(self.reqs)
+        return plan
+
+
+def run_device(args, wl, rank, world):
+    from paged_kv_cache_56_gb300.runtime import GraphStep
+
+    device = f"cuda:{torch.cuda.current_device()}"
+    steps_total = args.warmup + args.steps + args.e2e_steps
+    bench = Bench(wl, device, steps_total)
+    L, R, B = wl["L"], wl["repeat"], wl["B"]
+    Hq, Hkv, d, bs = wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
+    graph = not args.eager
+    # inputs for every step, resident in HBM before timing
+    inputs = [bench.step_inputs(s) for s in range(args.warmup + args.steps)]
+    gs = None
+    for s in range(args.warmup):
+        if gs is None:
+            plan = bench.cache.plan_step(bench.reqs)
+            bench.bufs.upload(plan)
+            gs = GraphStep(bench.cache, bench.bufs, bench.sm_scale, R)
+            q, k, v = inputs[s]
+            gs.q.copy_(q)
+            gs.k.copy_(k)
+            gs.v.copy_(v)
+            gs.run_eager()
+            bench.cache.commit_step(bench.reqs)
+            if graph:
+                gs.capture()
+        else:
+            bench.step(gs, *inputs[s], graph)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ctx_hist = []
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for s in range(args.steps):
+        plan = bench.step(gs, *inputs[args.warmup + s], graph)
+        ctx_hist.append(plan.ctx_lens.copy())
+    stop.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = gs.launches_per_step() * args.steps
+    ms = start.elapsed_time(stop)
+
+    # roofline: the attention calls alone, replayed back to back (same
+    # launches, same stream), timed with CUDA events
+    attn_reps = max(3, min(200, int(200.0 / max(ms / args.steps, 1e-3))))
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        a0.record()
+        for _ in range(attn_reps):
+            gs.attn_graph.replay()
+        a1.record()
+    else:
+        a0.record()
+        for _ in range(attn_reps):
+            gs._layers(attention_only=True)
+        a1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    attn_call_ms = a0.elapsed_time(a1) / (attn_reps * L * R)
+    attn_bytes = attention_bytes(ctx_hist[-1], Hq, Hkv, d, bs, wl["int8"])
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    step_bytes = sum(attention_bytes(c, Hq, Hkv, d, bs, wl["int8"]) for c in ctx_hist) * L * R
+    err = sum(lc.error_bits() for lc in bench.cache.layers)
+    if err:
+        raise RuntimeError(f"device error bits {err}")
+
+    # e2e: the same steps through host (pinned) buffers: H2D of the step's
+    # q/k/v into the graph's inputs, the step, D2H of the outputs -- all
+    # inside the timed region.
+    e2e = None
+    if args.e2e_steps > 0:
+        base = args.warmup + args.steps
+        host_in = []
+        for s in range(args.e2e_steps):
+            q, k, v = bench.step_inputs(base + s)
+            host_in.append(tuple(t.cpu().pin_memory() for t in (q, k, v)))
+        hout = torch.empty(gs.out.shape, dtype=gs.out.dtype).pin_memory()
+        e_ctx = []
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for s in range(args.e2e_steps):
+            plan = bench.step(gs, *host_in[s], graph)
+            hout.copy_(gs.out, non_blocking=True)
+            e_ctx.append(plan.ctx_lens.copy())
+        t1.record()
+        torch.cuda.synchronize()
+        e_ms = t0.elapsed_time(t1)
+        e_bytes = sum(attention_bytes(c, Hq, Hkv, d, bs, wl["int8"]) for c in e_ctx) * L * R
+        h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+        e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "tokens_per_s": round(B * args.e2e_steps / (e_ms * 1e-3), 1),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+               "ms_per_step": round(e_ms / args.e2e_steps, 4)}
+    return dict(ms=ms, attn_call_ms=attn_call_ms, attn_bytes=attn_bytes, step_bytes=step_bytes, clocks=clk,
+                launches=launches, split=bench.split, ctx=(int(ctx_hist[0].min()), int(ctx_hist[-1].max())),
+                e2e=e2e, graph=graph)
+
+
+# ---------------------------------------------------------------------------
+# the oracle arm (CPU)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, steps: int, budget_s: float = 20.0):
+    """Times the oracle on a bounded sample of the workload: decode steps of
+    the first layer's sequences (every query head), histories prebuilt
+    (untimed), each step = append one row + the oracle's context read +
+    fp64 attention. Returns (KV GB/s, tokens/s, sample description, cores)."""
+    from oracle.attention import decode_attention
+    from oracle.cache import SequenceHistory
+    from paged_kv_cache_56_gb300 import synth
+
+    B, Hq, Hkv, d, bs = wl["B"], wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
+    prior = wl["prior"] if isinstance(wl["prior"], list) else [wl["prior"]] * B
+    nseq = min(B, 2)
+    mult = lambda kind: (synth.outlier_multipliers(SEED, 0, kind, Hkv, d) if wl["outliers"] else
+                         synth.head_multipliers(SEED, 0, kind, Hkv) if wl["head_scale"] else None)
+    hists = []
+    for i in range(nseq):
+        h = SequenceHistory(Hkv, d, bs, wl["int8"])
+        pos = torch.arange(prior[i])
+        h.append(synth.kv_rows(SEED, 0, synth.KIND_K, 1000 + i, pos, Hkv, d, mult=mult(synth.KIND_K)).float().numpy(),
+                 synth.kv_rows(SEED, 0, synth.KIND_V, 1000 + i, pos, Hkv, d, mult=mult(synth.KIND_V)).float().numpy())
+        hists.append(h)
+    sm = 1.0 / math.sqrt(d)
+    qm = synth.head_multipliers(SEED, 0, synth.KIND_Q, Hq) if wl["head_scale"] else None
+    done_bytes, done_tokens, t_used = 0, 0, 0.0
+    for s in range(steps):
+        for i, h in enumerate(hists):
+            p = torch.tensor([h.n])
+            kr = synth.kv_rows(SEED, 0, synth.KIND_K, 1000 + i, p, Hkv, d, mult=mult(synth.KIND_K)).float().numpy()
+            vr = synth.kv_rows(SEED, 0, synth.KIND_V, 1000 + i, p, Hkv, d, mult=mult(synth.KIND_V)).float().numpy()
+            q = synth.q_rows(SEED, 0, s, [1000 + i], Hq, d, mult=qm)[0].float().numpy()
+            t0 = time.perf_counter()
+            h.append(kr, vr)
+            k, v = h.context()
+            decode_attention(q, k, v, sm)
+            t_used += time.perf_counter() - t0
+            done_bytes += attention_bytes([h.n], Hq, Hkv, d, bs, wl["int8"])
+            done_tokens += 1
+        if t_used > budget_s:
+            break
+    cores = torch.get_num_threads()
+    sample = (f"{s + 1} decode step(s) of {nseq} sequence(s) of one layer (all {Hq} query heads), "
+              f"context ~{max(prior[:nseq])}; scaled per byte")
+    return done_bytes / t_used / 1e9, done_tokens / t_used, sample, cores, t_used
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="tts_talker", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch each kernel from Python instead of a CUDA graph")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    peak, peak_kind = _peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, tps, sample, cores, used = oracle_sample(wl, steps=args.warmup + args.steps, budget_s=60.0)
+        line = {"impl": "reference", "metric": "paged decode-attention KV GB/s", "value": round(gbs, 4),
+                "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded counter-based generator)",
+                "config": {"workload": args.workload, "desc": wl["desc"]},
+                "tokens_per_s": round(tps, 3),
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample, "seconds": round(used, 2)},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    from paged_kv_cache_56_gb300 import build as _build
+    _build.build()
+    r = run_device(args, wl, rank, world)
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    ms_step = r["ms"] / args.steps
+    value = r["step_bytes"] * world / (r["ms"] * 1e-3) / 1e9
+    attn_avg_ms = r["attn_call_ms"]
+    achieved = r["attn_bytes"] / (attn_avg_ms * 1e-3) / 1e9
+    line = {
+        "metric": "paged decode-attention KV GB/s", "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 KV / bf16 q,out / fp32 accumulate" if wl["int8"] else "bf16 KV / fp32 accumulate",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": args.workload, "desc": wl["desc"], "split_tokens": r["split"],
+                   "ctx_range": list(r["ctx"]), "l2": "inputs larger than L2 (per-step KV >> 129 MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "CUDA graph per step" if r["graph"] else "eager"},
+        "tokens_per_s": round(wl["B"] * world / (ms_step * 1e-3), 1),
+        "hbm_frac_of_step": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "pkv_decode_attention (decode + split-K merge)",
+                     "bytes_per_launch": int(r["attn_bytes"]), "avg_launch_us": round(attn_avg_ms * 1e3, 2),
+                     "timing": "CUDA events over back-to-back replays of the step's attention calls"},
+        "clocks": r["clocks"],
+        "gpu_launches": r["launches"],
+        "e2e": r["e2e"],
+    }
+    if not args.no_cpu_baseline:
+        gbs, tps, sample, cores, used = oracle_sample(wl, steps=1000, budget_s=15.0)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": round(used, 2), "tokens_per_s": round(tps, 3)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

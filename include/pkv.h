@@ -64,7 +64,7 @@ extern "C" {
 #define PKV_DTYPE_INT8 1
 
 /* Compiled shapes: head_dim in {64, 128}; block_size in {16, 64};
- * Hq / Hkv in {1, 2, 4} for head_dim 128 and {1, 2, 4, 8} for head_dim 64. */
+ * Hq / Hkv in {1, 2, 4, 8}. */
 
 /* ======================================================================== */
 /* Host block allocator ([D] §4.2; [A] §1.2; [B] §3.2; [E] §2.1)            */

@@ -10,13 +10,12 @@
 //     engine, one elected lane, completion on an mbarrier), gathering tiles
 //     through the block table. A (block, kv head) tile is contiguous in the
 //     [num_blocks][Hkv][bs][d] pools, so every copy is one linear transfer;
-//   * a token is spread over d/16 lanes, each holding 16 of its dims; QK and
-//     PV run on packed fp32 FMAs (f32x2); INT8 values are converted exactly
-//     in registers and the per-block scales are applied to the scores and to
-//     the softmax weights, not per element;
-//   * fp32 online softmax in base 2 (scores pre-multiplied by log2 e), one
-//     state per group of lanes, merged across lanes with shuffles and across
-//     warps through shared memory at the end.
+//   * QK and PV of each 16-token tile run on tensor cores (mma.m16n8k16,
+//     fp32 accumulate) straight from registers: INT8 codes are converted
+//     exactly to f16 in registers, and the per-block scales are applied to
+//     the scores and to the softmax weights, not per element;
+//   * fp32 online softmax in base 2 (scores pre-multiplied by log2 e); each
+//     warp keeps its own state, merged across warps through shared memory.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -66,13 +65,10 @@ struct DecodeTraits {
     static constexpr int kRowBytes = D * kElemBytes;
     static constexpr int kTileBytes = kTile * kRowBytes;  // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = INT8 ? 6 : 4;
-    static constexpr int kLPT = D / 16;         // lanes per token
-    static constexpr int kTPW = 32 / kLPT;      // tokens per warp pass
-    static constexpr int kIters = kTile / kTPW; // passes per tile
+    static constexpr int kStages = INT8 ? 4 : 3;
 };
 
-// Shared-memory bytes one decode CTA needs.
+// Shared-memory bytes of a decode CTA before its block table.
 template <int D, int G, bool INT8>
 constexpr size_t decode_smem_fixed() {
     using T = DecodeTraits<D, INT8>;
@@ -82,143 +78,270 @@ constexpr size_t decode_smem_fixed() {
          + size_t(kWarps) * G * 2 * 4;                    // merge: m, l
 }
 
-// Lane-to-dimension map. Lane `sub` of a token holds 16 dims:
-//   INT8 kernels: dims sub*16 .. sub*16+15 (one 16-byte int8 chunk);
-//   BF16 kernels: dims sub*8 .. sub*8+7 and D/2 + sub*8 .. +7 (two 16-byte
-//   chunks, so that eight consecutive lanes read 128 contiguous bytes).
-template <int D, bool INT8>
-__device__ __forceinline__ int lane_dim(int sub, int i) {
-    if (INT8) return sub * 16 + i;
-    return i < 8 ? sub * 8 + i : D / 2 + sub * 8 + (i - 8);
+// ---- tensor-core tile math ---------------------------------------------------
+// One warp computes a 16-token tile with mma.m16n8k16 (fp32 accumulate):
+//   S   [16 tok x 8 heads] = K [16 tok x D] . Q^T [D x 8 heads]
+//   O^T [D x 8 heads]     += V^T [D x 16 tok] . P^T [16 tok x 8 heads]
+// Lane (g = lane / 4, t = lane % 4). The GQA group (G <= 8 query heads) is the
+// 8-wide N dimension; heads >= G are zero columns.
+// K operand: lane holds tokens g and g+8; the MMA's k index is permuted so
+// that lane t's dims for all k-steps are the contiguous run [t*D/4, t*D/4 +
+// D/4) (k-step ks uses dims t*D/4 + 4ks + 0..3), the same permutation on Q.
+// V operand: m-tile m's rows are dims g*D/8 + 2m (row g) and g*D/8 + 2m + 1
+// (row g+8), so lane g reads the contiguous run [g*D/8, g*D/8 + D/8) of
+// tokens 2t, 2t+1, 2t+8, 2t+9; the output row of a lane is that run too.
+// P^T comes from S by an in-register 8x8 transpose (movmatrix).
+// INT8 codes are exact in f16 (x + 1152 = f16 bits 0x6400 | (x ^ 0x80), then
+// subtract 1152); bf16 caches multiply in bf16.
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    if (F16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 16 bf16 values of a global row at this lane's dims -> fp32 pairs.
-template <int D, bool INT8>
-__device__ __forceinline__ void load_bf16_dims_global(const uint16_t* row, int sub, float2 (&x)[8]) {
-    uint4 a, b;
-    if (INT8) {
-        a = ldg128(row + sub * 16);
-        b = ldg128(row + sub * 16 + 8);
-    } else {
-        a = ldg128(row + sub * 8);
-        b = ldg128(row + D / 2 + sub * 8);
-    }
-    x[0] = bf16x2_to_f2(a.x); x[1] = bf16x2_to_f2(a.y); x[2] = bf16x2_to_f2(a.z); x[3] = bf16x2_to_f2(a.w);
-    x[4] = bf16x2_to_f2(b.x); x[5] = bf16x2_to_f2(b.y); x[6] = bf16x2_to_f2(b.z); x[7] = bf16x2_to_f2(b.w);
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
-// Row loader for a staged tile in shared memory.
-template <int D, bool INT8>
-struct SmemTile {
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if (F16) asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub1152(uint32_t x) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64806480u));  // 1152 = f16 0x6480
+    return r;
+}
+
+// int8 dims (d, d+1, d+2, d+3) of one word -> f16x2 (d, d+1), (d+2, d+3).
+__device__ __forceinline__ void s8_pairs(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    lo = hsub1152(__byte_perm(u, 0x64646464u, 0x4140));
+    hi = hsub1152(__byte_perm(u, 0x64646464u, 0x4342));
+}
+
+// int8 words of two tokens (same dims d..d+3) -> f16x2 (t0[d+i], t1[d+i]), i = 0..3.
+__device__ __forceinline__ void s8_interleave(uint32_t w0, uint32_t w1, uint32_t (&r)[4]) {
+    const uint32_t x = __byte_perm(w0, w1, 0x5140) ^ 0x80808080u;
+    const uint32_t y = __byte_perm(w0, w1, 0x7362) ^ 0x80808080u;
+    r[0] = hsub1152(__byte_perm(x, 0x64646464u, 0x4140));
+    r[1] = hsub1152(__byte_perm(x, 0x64646464u, 0x4342));
+    r[2] = hsub1152(__byte_perm(y, 0x64646464u, 0x4140));
+    r[3] = hsub1152(__byte_perm(y, 0x64646464u, 0x4342));
+}
+
+template <int D, bool I8>
+struct Geom {
+    static constexpr int kE = I8 ? 1 : 2;    // bytes per element
+    static constexpr int kRow = D * kE;      // bytes per token row
+    static constexpr int kKB = D / 4 * kE;   // K bytes a lane reads per token
+    static constexpr int kKW = kKB / 4;      // ... as words
+    static constexpr int kVB = D / 8 * kE;   // V bytes a lane reads per token
+    static constexpr int kVW = kVB / 4;
+    static constexpr int kSteps = D / 16;    // QK k-steps = PV m-tiles
+};
+
+// 16-byte / 8-byte row loads from a staged tile (shared) or from global rows.
+struct SmemRows {
     uint32_t base;
-    __device__ __forceinline__ void load(int r, int sub, float2 (&x)[8]) const {
-        using T = DecodeTraits<D, INT8>;
-        const uint32_t row = base + uint32_t(r) * T::kRowBytes;
-        if (INT8) {
-            uint4 w = lds128(row + sub * 16);
-            s8x4_to_f4(w.x, x[0], x[1]);
-            s8x4_to_f4(w.y, x[2], x[3]);
-            s8x4_to_f4(w.z, x[4], x[5]);
-            s8x4_to_f4(w.w, x[6], x[7]);
-        } else {
-            uint4 a = lds128(row + sub * 16);
-            uint4 b = lds128(row + D + sub * 16);
-            x[0] = bf16x2_to_f2(a.x); x[1] = bf16x2_to_f2(a.y); x[2] = bf16x2_to_f2(a.z); x[3] = bf16x2_to_f2(a.w);
-            x[4] = bf16x2_to_f2(b.x); x[5] = bf16x2_to_f2(b.y); x[6] = bf16x2_to_f2(b.z); x[7] = bf16x2_to_f2(b.w);
-        }
+    int row;  // bytes
+    __device__ __forceinline__ uint4 ld16(int r, int off) const { return lds128(base + uint32_t(r * row + off)); }
+    __device__ __forceinline__ uint2 ld8(int r, int off) const {
+        uint2 v;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(base + uint32_t(r * row + off)));
+        return v;
+    }
+};
+struct GmemRows {
+    const uint8_t* base;
+    int row;
+    __device__ __forceinline__ uint4 ld16(int r, int off) const { return ldg128(base + size_t(r) * row + off); }
+    __device__ __forceinline__ uint2 ld8(int r, int off) const {
+        return *reinterpret_cast<const uint2*>(base + size_t(r) * row + off);
     }
 };
 
-// Row loader for bf16 rows in global memory (the INT8 cache's tail block).
-template <int D, bool INT8>
-struct GlobalBf16Rows {
-    const uint16_t* base;  // row 0
-    __device__ __forceinline__ void load(int r, int sub, float2 (&x)[8]) const {
-        load_bf16_dims_global<D, INT8>(base + size_t(r) * D, sub, x);
+template <int NB, class Rows>
+__device__ __forceinline__ void load_run(const Rows& R, int r, int off, uint32_t* w) {
+    if constexpr (NB % 16 == 0) {
+#pragma unroll
+        for (int c = 0; c < NB / 16; ++c) {
+            const uint4 v = R.ld16(r, off + c * 16);
+            w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+    } else {
+        static_assert(NB == 8, "8- or 16k-byte runs");
+        const uint2 v = R.ld8(r, off);
+        w[0] = v.x; w[1] = v.y;
     }
+}
+
+// Per-warp online-softmax state: heads 2t and 2t+1 (replicated over g);
+// l is this lane's partial sum over its tokens; acc holds O^T fragments.
+template <int D>
+struct WarpState {
+    float m[2], l[2];
+    float acc[D / 16][4];
 };
 
-// One 16-token tile: scores, online-softmax update, weighted V accumulation.
-// nvalid < 16 masks the tile's last rows (their scores become -inf and their
-// V rows are zeroed, so stale or uninitialised rows cannot leak NaNs in).
-template <int D, int G, class Loader>
-__device__ __forceinline__ void tile_step(const Loader& kl, const Loader& vl, int nvalid, float ksc,
-                                          float vsc, int tk, int sub, const float2 (&q2)[G][8],
-                                          float (&m)[G], float (&l)[G], float2 (&o2)[G][8]) {
-    constexpr int LPT = D / 16, TPW = 32 / LPT, ITERS = kTile / TPW;
-    float s[ITERS][G];
+// One 16-token tile. nvalid < 16 masks the last rows: their scores become
+// -inf and their V values 0, so stale or uninitialised rows cannot leak NaNs.
+// hs[j]: log2-domain logit factor of head 2t+j; ksc/vsc: the block's scales.
+template <int D, bool I8, class Rows>
+__device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvalid, float ksc, float vsc,
+                                         const uint32_t (&qf)[D / 16][2], const float (&hs)[2], int g, int t,
+                                         WarpState<D>& st) {
+    using Gm = Geom<D, I8>;
+    constexpr bool F16 = I8;
+    // ---- S = K . Q^T
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        uint32_t k0[Gm::kKW], k1[Gm::kKW];
+        load_run<Gm::kKB>(K, g, t * Gm::kKB, k0);
+        load_run<Gm::kKB>(K, g + 8, t * Gm::kKB, k1);
 #pragma unroll
-    for (int it = 0; it < ITERS; ++it) {
-        float2 x[8];
-        kl.load(it * TPW + tk, sub, x);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a = __ffma2_rn(q2[g][i], x[i], a);
-            s[it][g] = a.x + a.y;
+        for (int ks = 0; ks < Gm::kSteps; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            if (I8) {
+                s8_pairs(k0[ks], a0, a2);
+                s8_pairs(k1[ks], a1, a3);
+            } else {
+                a0 = k0[2 * ks]; a2 = k0[2 * ks + 1];
+                a1 = k1[2 * ks]; a3 = k1[2 * ks + 1];
+            }
+            mma16816<F16>(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
     }
-#pragma unroll
-    for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it)
-#pragma unroll
-            for (int g = 0; g < G; ++g) s[it][g] += __shfl_xor_sync(kFull, s[it][g], off);
-
+    const float f0 = ksc * hs[0], f1 = ksc * hs[1];
+    s[0] *= f0; s[1] *= f1; s[2] *= f0; s[3] *= f1;
     const bool full = nvalid >= kTile;
-#pragma unroll
-    for (int it = 0; it < ITERS; ++it) {
-        const bool ok = full || (it * TPW + tk) < nvalid;
-#pragma unroll
-        for (int g = 0; g < G; ++g) s[it][g] = ok ? s[it][g] * ksc : -INFINITY;
+    if (!full) {
+        if (g >= nvalid) s[0] = s[1] = -INFINITY;
+        if (g + 8 >= nvalid) s[2] = s[3] = -INFINITY;
     }
+    // ---- online softmax over the 16 tokens of each head
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    mx0 = fmaxf(mx0, st.m[0]);
+    mx1 = fmaxf(mx1, st.m[1]);
+    if (__any_sync(kFull, (mx0 > st.m[0]) | (mx1 > st.m[1]))) {
+        const float c0 = fast_exp2(st.m[0] - mx0), c1 = fast_exp2(st.m[1] - mx1);
+        st.m[0] = mx0;
+        st.m[1] = mx1;
+        st.l[0] *= c0;
+        st.l[1] *= c1;
+#pragma unroll
+        for (int m = 0; m < Gm::kSteps; ++m) {
+            st.acc[m][0] *= c0; st.acc[m][1] *= c1; st.acc[m][2] *= c0; st.acc[m][3] *= c1;
+        }
+    }
+    const float p0 = fast_exp2(s[0] - st.m[0]), p1 = fast_exp2(s[1] - st.m[1]);
+    const float p2 = fast_exp2(s[2] - st.m[0]), p3 = fast_exp2(s[3] - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    const uint32_t b0 = movmatrix_t(pack2<F16>(p0 * vsc, p1 * vsc));
+    const uint32_t b1 = movmatrix_t(pack2<F16>(p2 * vsc, p3 * vsc));
+    // ---- O^T += V^T . P^T
+    uint32_t v0[Gm::kVW], v1[Gm::kVW], v2[Gm::kVW], v3[Gm::kVW];
+    load_run<Gm::kVB>(V, 2 * t, g * Gm::kVB, v0);
+    load_run<Gm::kVB>(V, 2 * t + 1, g * Gm::kVB, v1);
+    load_run<Gm::kVB>(V, 2 * t + 8, g * Gm::kVB, v2);
+    load_run<Gm::kVB>(V, 2 * t + 9, g * Gm::kVB, v3);
+    if (!full) {
+#pragma unroll
+        for (int i = 0; i < Gm::kVW; ++i) {
+            if (2 * t >= nvalid) v0[i] = 0u;
+            if (2 * t + 1 >= nvalid) v1[i] = 0u;
+            if (2 * t + 8 >= nvalid) v2[i] = 0u;
+            if (2 * t + 9 >= nvalid) v3[i] = 0u;
+        }
+    }
+    if (I8) {
+#pragma unroll
+        for (int j = 0; j < Gm::kVW; ++j) {
+            uint32_t r01[4], r23[4];
+            s8_interleave(v0[j], v1[j], r01);
+            s8_interleave(v2[j], v3[j], r23);
+            mma16816<true>(st.acc[2 * j], r01[0], r01[1], r23[0], r23[1], b0, b1);
+            mma16816<true>(st.acc[2 * j + 1], r01[2], r01[3], r23[2], r23[3], b0, b1);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < Gm::kVW; ++j) {
+            const uint32_t a0 = __byte_perm(v0[j], v1[j], 0x5410), a1 = __byte_perm(v0[j], v1[j], 0x7632);
+            const uint32_t a2 = __byte_perm(v2[j], v3[j], 0x5410), a3 = __byte_perm(v2[j], v3[j], 0x7632);
+            mma16816<false>(st.acc[j], a0, a1, a2, a3, b0, b1);
+        }
+    }
+}
 
-    float mnew[G];
-    bool up = false;
+// Q^T fragments of head g (zero for g >= G): dims t*D/4 + 4ks + {0,1} and
+// {2,3} of the query row. F16: the row is scaled by 2^e (e per head, chosen so
+// that max|q| * 2^e lies in [2^14, 2^15) -- exact, and safe from f16
+// overflow); returns e. BF16: the raw row, e = 0.
+template <int D, int G, bool F16>
+__device__ __forceinline__ int load_q_frags(const uint16_t* qrow, int g, int t, uint32_t (&qf)[D / 16][2]) {
+    constexpr int NW = D / 8;  // bf16 words in a lane's D/4 dims
+    uint32_t w[NW];
+    if (g < G) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float mx = m[g];
+        for (int c = 0; c < NW / 4; ++c) {
+            const uint4 v = ldg128(qrow + t * (D / 4) + c * 8);
+            w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+    } else {
 #pragma unroll
-        for (int it = 0; it < ITERS; ++it) mx = fmaxf(mx, s[it][g]);
-        mnew[g] = mx;
-        up |= mx > m[g];
+        for (int i = 0; i < NW; ++i) w[i] = 0u;
     }
-    if (__any_sync(kFull, up)) {
+    if (!F16) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float c = fast_exp2(m[g] - mnew[g]);
-            m[g] = mnew[g];
-            l[g] *= c;
-            const float2 c2 = make_float2(c, c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o2[g][i] = __fmul2_rn(o2[g][i], c2);
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qf[ks][0] = w[2 * ks];
+            qf[ks][1] = w[2 * ks + 1];
         }
+        return 0;
     }
+    float mx = 0.f;
 #pragma unroll
-    for (int it = 0; it < ITERS; ++it)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float pr = fast_exp2(s[it][g] - m[g]);
-            l[g] += pr;
-            s[it][g] = pr * vsc;
-        }
-
-#pragma unroll
-    for (int it = 0; it < ITERS; ++it) {
-        float2 x[8];
-        vl.load(it * TPW + tk, sub, x);
-        if (!full && (it * TPW + tk) >= nvalid) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = make_float2(0.f, 0.f);
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float2 p2 = make_float2(s[it][g], s[it][g]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o2[g][i] = __ffma2_rn(p2, x[i], o2[g][i]);
-        }
+    for (int i = 0; i < NW; ++i) {
+        const float2 f = bf16x2_to_f2(w[i]);
+        mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    int e = 0;
+    if (mx > 0.f) e = 15 - (int((__float_as_uint(mx) >> 23) & 0xFF) - 126);
+    e = max(-100, min(100, e));
+    const float sc = ldexpf(1.0f, e);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const float2 a = bf16x2_to_f2(w[2 * ks]), b = bf16x2_to_f2(w[2 * ks + 1]);
+        qf[ks][0] = pack2<true>(a.x * sc, a.y * sc);
+        qf[ks][1] = pack2<true>(b.x * sc, b.y * sc);
+    }
+    return e;
 }
 
 // Waits for an mbarrier phase for at most ~1 s of GPU time.
@@ -237,8 +360,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
 
 template <int D, int G, bool INT8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+    static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
     using T = DecodeTraits<D, INT8>;
-    constexpr int LPT = T::kLPT, STAGES = T::kStages;
+    using Gm = Geom<D, INT8>;
+    constexpr int STAGES = T::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
@@ -249,7 +374,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 
     const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sub = lane % LPT, tk = lane / LPT;
+    const int g = lane >> 2, t = lane & 3;
 
     int ctx = p.ctx_lens[b];
     if (ctx < 0 || ctx > p.max_blocks * p.bs) {
@@ -317,23 +442,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         }
     }
 
-    float2 q2[G][8];
+    const uint16_t* qbase = p.q + (size_t(b) * p.Hq + size_t(kvh) * G) * D;
+    uint32_t qf[D / 16][2];
+    const int qe = load_q_frags<D, G, INT8>(qbase + size_t(g) * D, g, t, qf);
+    float hs[2];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        load_bf16_dims_global<D, INT8>(p.q + (size_t(b) * p.Hq + kvh * G + g) * D, sub, q2[g]);
-        const float2 qs = make_float2(p.qscale, p.qscale);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q2[g][i] = __fmul2_rn(q2[g][i], qs);
+    for (int jj = 0; jj < 2; ++jj) {
+        const int eh = __shfl_sync(kFull, qe, ((2 * t + jj) & 7) * 4);
+        hs[jj] = p.qscale * ldexpf(1.0f, -eh);
     }
-    float m[G], l[G];
-    float2 o2[G][8];
+    WarpState<D> st;
+    st.m[0] = st.m[1] = -1e30f;
+    st.l[0] = st.l[1] = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -1e30f;
-        l[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o2[g][i] = make_float2(0.f, 0.f);
-    }
+    for (int m = 0; m < D / 16; ++m) st.acc[m][0] = st.acc[m][1] = st.acc[m][2] = st.acc[m][3] = 0.f;
     __syncthreads();
 
     // ---- main loop over this warp's pool tiles ----------------------------------
@@ -355,8 +477,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             ksc = sc.x;
             vsc = sc.y;
         }
-        const SmemTile<D, INT8> kt{stage_of(s)}, vt{stage_of(s) + T::kTileBytes};
-        tile_step<D, G>(kt, vt, nvalid, ksc, vsc, tk, sub, q2, m, l, o2);
+        const SmemRows kr{stage_of(s), Gm::kRow}, vr{stage_of(s) + T::kTileBytes, Gm::kRow};
+        mma_tile<D, INT8>(kr, vr, nvalid, ksc, vsc, qf, hs, g, t, st);
         __syncwarp();
         const int nxt = tile + STAGES * kWarps;
         if (lane == 0 && nxt < nt) {
@@ -381,51 +503,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             if (slot < 0 || slot >= p.max_slots) {
                 if (tid == 0) report(p.err, kErrSlot);
             } else {
+                uint32_t qb[D / 16][2];
+                (void)load_q_frags<D, G, false>(qbase + size_t(g) * D, g, t, qb);
+                const float hb[2] = {p.qscale, p.qscale};
                 const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull);
-                const uint16_t* kt = static_cast<const uint16_t*>(p.k_tail) + rbase * D;
-                const uint16_t* vt = static_cast<const uint16_t*>(p.v_tail) + rbase * D;
+                const uint8_t* kt = static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2;
+                const uint8_t* vt = static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2;
                 for (int tt = warp; tt * kTile < ntail; tt += kWarps) {
-                    const GlobalBf16Rows<D, INT8> kr{kt + size_t(tt) * kTile * D};
-                    const GlobalBf16Rows<D, INT8> vr{vt + size_t(tt) * kTile * D};
-                    tile_step<D, G>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, tk, sub, q2, m, l, o2);
+                    const GmemRows kr{kt + size_t(tt) * kTile * D * 2, D * 2};
+                    const GmemRows vr{vt + size_t(tt) * kTile * D * 2, D * 2};
+                    mma_tile<D, false>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, qb, hb, g, t, st);
                 }
             }
         }
     }
 
-    // ---- merge the lane groups of this warp ---------------------------------
+    // ---- merge: lanes of a warp hold disjoint dims; sum l over the 8 g lanes
 #pragma unroll
-    for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float mb = __shfl_xor_sync(kFull, m[g], off);
-            const float lb = __shfl_xor_sync(kFull, l[g], off);
-            const float mm = fmaxf(m[g], mb);
-            const float ca = fast_exp2(m[g] - mm), cb = fast_exp2(mb - mm);
-            m[g] = mm;
-            l[g] = l[g] * ca + lb * cb;
-            const float2 ca2 = make_float2(ca, ca), cb2 = make_float2(cb, cb);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float2 ob;
-                ob.x = __shfl_xor_sync(kFull, o2[g][i].x, off);
-                ob.y = __shfl_xor_sync(kFull, o2[g][i].y, off);
-                o2[g][i] = __ffma2_rn(o2[g][i], ca2, __fmul2_rn(ob, cb2));
-            }
-        }
+    for (int off = 4; off < 32; off <<= 1) {
+        st.l[0] += __shfl_xor_sync(kFull, st.l[0], off);
+        st.l[1] += __shfl_xor_sync(kFull, st.l[1], off);
     }
-    if (tk == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float* dst = mo + (warp * G + g) * D;
+    for (int jj = 0; jj < 2; ++jj) {
+        const int h = 2 * t + jj;
+        if (h < G) {
+            float* dst = mo + (warp * G + h) * D + g * (D / 8);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                dst[lane_dim<D, INT8>(sub, 2 * i)] = o2[g][i].x;
-                dst[lane_dim<D, INT8>(sub, 2 * i + 1)] = o2[g][i].y;
+            for (int m = 0; m < D / 16; ++m) {
+                dst[2 * m] = st.acc[m][jj];
+                dst[2 * m + 1] = st.acc[m][2 + jj];
             }
-            if (sub == 0) {
-                mml[(warp * G + g) * 2] = m[g];
-                mml[(warp * G + g) * 2 + 1] = l[g];
+            if (g == 0) {
+                mml[(warp * G + h) * 2] = st.m[jj];
+                mml[(warp * G + h) * 2 + 1] = st.l[jj];
             }
         }
     }
@@ -433,18 +544,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 
     // ---- merge the warps and write ---------------------------------------------
     for (int e = tid; e < G * D; e += kThreads) {
-        const int g = e / D, dim = e % D;
+        const int h = e / D, dim = e % D;
         float mm = -1e30f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, mml[(w * G + g) * 2]);
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, mml[(w * G + h) * 2]);
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float c = fast_exp2(mml[(w * G + g) * 2] - mm);
-            L += mml[(w * G + g) * 2 + 1] * c;
-            O += mo[(w * G + g) * D + dim] * c;
+            const float c = fast_exp2(mml[(w * G + h) * 2] - mm);
+            L += mml[(w * G + h) * 2 + 1] * c;
+            O += mo[(w * G + h) * D + dim] * c;
         }
-        const size_t hrow = size_t(b) * p.Hq + kvh * G + g;
+        const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
         if (SPLIT) {
             const size_t w = hrow * p.max_splits + j;
             p.ws_o[w * D + dim] = O;

@@ -148,7 +148,7 @@ static int check_desc(const pkv_cache_desc* c) {
     if (c->block_size != 16 && c->block_size != 64) return PKV_ERR_UNSUPPORTED;
     if (c->num_q_heads % c->num_kv_heads) return PKV_ERR_UNSUPPORTED;
     const int g = c->num_q_heads / c->num_kv_heads;
-    const bool g_ok = g == 1 || g == 2 || g == 4 || (g == 8 && c->head_dim == 64);
+    const bool g_ok = g == 1 || g == 2 || g == 4 || g == 8;
     if (!g_ok) return PKV_ERR_UNSUPPORTED;
     if (c->dtype == PKV_DTYPE_INT8) {
         if (!c->scales || !c->k_tail || !c->v_tail || c->max_slots <= 0) return PKV_ERR_INVALID;
@@ -182,9 +182,7 @@ static int dispatch_g(int g, const DecodeParams& p, dim3 grid, size_t smem, cuda
         case 1: return launch_decode_t<D, 1, INT8, SPLIT>(p, grid, smem, st);
         case 2: return launch_decode_t<D, 2, INT8, SPLIT>(p, grid, smem, st);
         case 4: return launch_decode_t<D, 4, INT8, SPLIT>(p, grid, smem, st);
-        case 8:
-            if constexpr (D == 64) return launch_decode_t<D, 8, INT8, SPLIT>(p, grid, smem, st);
-            return PKV_ERR_UNSUPPORTED;
+        case 8: return launch_decode_t<D, 8, INT8, SPLIT>(p, grid, smem, st);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }

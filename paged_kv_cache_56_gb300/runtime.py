@@ -309,3 +309,66 @@ def decode_step(cache: PagedKVCache, bufs: StepBuffers, req_ids, q, k_new, v_new
     run_layers(cache, bufs, q, k_new, v_new, out, sm_scale, "auto", plan, stream)
     cache.commit_step(req_ids)
     return plan
+
+
+class GraphStep:
+    """The kernel launches of one decode step, captured once as a CUDA graph
+    ("离开 N 卡后的真实世界" §2: graph capture turns a decode step's dozens of
+    small launches into one submission).
+
+    The graph reads its inputs from static device buffers -- ``q`` [L*R, B,
+    Hq, d], ``k``/``v`` [L, B, Hkv, d] -- and the StepBuffers control arrays,
+    and writes ``out`` [L*R, B, Hq, d]; each layer's attention runs R times
+    (R > 1 re-reads the same layer's cache with R different queries). The
+    quantize kernel is always launched over a -1-padded fill list so that the
+    graph does not change from step to step. The batch size is fixed at
+    capture time.
+    """
+
+    def __init__(self, cache: PagedKVCache, bufs: StepBuffers, sm_scale: float, repeat: int = 1):
+        self.cache, self.bufs, self.sm_scale, self.R = cache, bufs, sm_scale, repeat
+        B, dev = bufs.B, cache.device
+        if B == 0:
+            raise ValueError("upload a plan before capturing")
+        L = cache.L
+        self.q = torch.zeros((L * repeat, B, cache.hq, cache.d), dtype=torch.bfloat16, device=dev)
+        self.k = torch.zeros((L, B, cache.hkv, cache.d), dtype=torch.bfloat16, device=dev)
+        self.v = torch.zeros((L, B, cache.hkv, cache.d), dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros((L * repeat, B, cache.hq, cache.d), dtype=torch.bfloat16, device=dev)
+        self.graph = None
+        self.attn_graph = None
+
+    def launches_per_step(self) -> int:
+        per_attn = 2 if self.bufs.split_tokens else 1
+        return self.cache.L * (1 + (1 if self.cache.int8 else 0) + self.R * per_attn)
+
+    def _layers(self, attention_only: bool = False) -> None:
+        c, b = self.cache, self.bufs
+        B = b.B
+        for li, lc in enumerate(c.layers):
+            if not attention_only:
+                pkv.pkv_append_kv(lc.desc, self.k[li], self.v[li], b.blk[:B], b.off[:B], b.slot[:B])
+                if c.int8:
+                    pkv.pkv_quantize_full_blocks(lc.desc, b.fill[:B], b.slot[:B])
+            for r in range(self.R):
+                qi = li * self.R + r
+                pkv.pkv_decode_attention(lc.desc, self.q[qi], b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
+                                         self.out[qi], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml)
+
+    def run_eager(self) -> None:
+        self._layers()
+
+    def capture(self) -> None:
+        """Captures the step (and an attention-only variant used for timing).
+        Call after one eager step so every kernel attribute is already set."""
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._layers()
+        self.attn_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.attn_graph):
+            self._layers(attention_only=True)
+        torch.cuda.synchronize()
+
+    def replay(self) -> None:
+        self.graph.replay()

@@ -51,7 +51,7 @@ def _desc(**kw):
     (dict(head_dim=96), pkv.PKV_ERR_UNSUPPORTED),
     (dict(block_size=32), pkv.PKV_ERR_UNSUPPORTED),
     (dict(num_q_heads=6, num_kv_heads=4), pkv.PKV_ERR_UNSUPPORTED),
-    (dict(num_q_heads=16, num_kv_heads=2), pkv.PKV_ERR_UNSUPPORTED),   # G = 8 at d = 128
+    (dict(num_q_heads=32, num_kv_heads=2), pkv.PKV_ERR_UNSUPPORTED),   # G = 16
     (dict(k_pool=None), pkv.PKV_ERR_INVALID),
     (dict(k_pool=24), pkv.PKV_ERR_INVALID),                           # misaligned pool
     (dict(dtype=7), pkv.PKV_ERR_INVALID),
