@@ -149,9 +149,9 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Bench:
-    def __init__(self, wl: dict, device: str, steps_total: int):
+    def __init__(self, wl: dict, device: str, steps_total: int, split=None, fused_merge=True):
         from paged_kv_cache_56_gb300 import synth
-        from paged_kv_cache_56_gb300.runtime import PagedKVCache, StepBuffers, choose_split_tokens, prefill
+        from paged_kv_cache_56_gb300.runtime import PagedKVCache, StepBuffers, plan_split_tokens, prefill
 
         self.wl = wl
         self.synth = synth
@@ -165,9 +165,8 @@ class Bench:
         self.cache = PagedKVCache(L, wl["num_blocks"], Hq, Hkv, d, bs, wl["int8"], max_slots=B,
                                   max_blocks_per_seq=max_blocks, device=device,
                                   initial_order=synth.permutation(SEED, wl["num_blocks"]))
-        props = torch.cuda.get_device_properties(torch.device(device))
-        self.split = choose_split_tokens(B, Hkv, max(prior) + steps_total + 1, bs, props.multi_processor_count)
-        self.bufs = StepBuffers(self.cache, B, self.split)
+        self.split = plan_split_tokens(self.cache, B, max(prior) + steps_total + 1) if split is None else split
+        self.bufs = StepBuffers(self.cache, B, self.split, fused_merge=fused_merge)
         for r, n in zip(self.reqs, prior):
             self.cache.add_sequence(r, -(-n // bs))
         for li in range(L):
@@ -226,7 +225,7 @@ def run_device(args, wl, rank, world):
 
     device = f"cuda:{torch.cuda.current_device()}"
     steps_total = args.warmup + args.steps + args.e2e_steps
-    bench = Bench(wl, device, steps_total)
+    bench = Bench(wl, device, steps_total, split=args.split, fused_merge=not args.separate_merge)
     L, R, B = wl["L"], wl["repeat"], wl["B"]
     Hq, Hkv, d, bs = wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
     graph = not args.eager
@@ -389,6 +388,8 @@ def main():
     ap.add_argument("--workload", default="tts_talker", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch each kernel from Python instead of a CUDA graph")
+    ap.add_argument("--split", type=int, default=None, help="split_tokens (default: sized to one wave)")
+    ap.add_argument("--separate-merge", action="store_true", help="merge split-K partials in a second kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -435,7 +436,8 @@ def main():
         "config": {"workload": args.workload, "desc": wl["desc"], "split_tokens": r["split"],
                    "ctx_range": list(r["ctx"]), "l2": "inputs larger than L2 (per-step KV >> 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph per step" if r["graph"] else "eager"},
+                   "launch": "CUDA graph per step" if r["graph"] else "eager",
+                   "split_merge": "separate kernel" if args.separate_merge else "fused (last split merges)"},
         "tokens_per_s": round(wl["B"] * world / (ms_step * 1e-3), 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

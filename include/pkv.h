@@ -190,18 +190,29 @@ int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const v
  * partly filled block) are read from the bf16 tail of slot slots[b].
  * Accumulation is fp32; out is bf16. ctx_lens[b] == 0 gives a zero row.
  *
- * split_tokens == 0: one pass per (b, kv_head); ws_o, ws_ml unused (NULL ok).
+ * split_tokens == 0: one pass per (b, kv_head); the workspace is unused (NULL ok).
  * split_tokens > 0 (a multiple of block_size and of 16): the context is cut
  *   into chunks of split_tokens tokens, computed independently into the
- *   caller's workspace, then merged by the split-K reduce (same stream).
- *   Needs max_splits * split_tokens >= max_blocks * block_size and
+ *   caller's workspace and then merged. Needs
+ *   max_splits * split_tokens >= max_blocks * block_size and
  *   ws_o  >= pkv_splitk_ws_o_bytes(B, Hq, d, max_splits),
  *   ws_ml >= pkv_splitk_ws_ml_bytes(B, Hq, max_splits), 16-byte aligned.
+ *   ws_count NULL: the merge is a second kernel (pkv_splitk_reduce) on the
+ *   same stream. ws_count non-NULL: device int32 [B][Hkv], all zero before
+ *   the first call; the last split of each (b, kv_head) to finish merges in
+ *   the same kernel and sets its counter back to zero, so the array stays
+ *   ready for the next call. Calls sharing a workspace must not overlap.
  * slots may be NULL in BF16 mode. */
 int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
                          int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                          int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
-                         float* ws_o, float* ws_ml, void* out, void* stream);
+                         float* ws_o, float* ws_ml, int32_t* ws_count, void* out, void* stream);
+
+/* CTAs of the decode kernel for this cache shape that fit on one SM at once
+ * (registers and shared memory), for a given split_tokens (0 = none) and
+ * max_blocks; a caller sizes its splits so that B * Hkv * splits fills
+ * SMs x this number. Returns a negative status on invalid arguments. */
+int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_t max_blocks);
 
 /* Split-K merge of partial softmax states (the combination rule of a
  * softmax over a partition of the context; the pages' tiled softmax, [C] §2).

@@ -53,6 +53,7 @@ struct DecodeParams {
     uint16_t* out;
     float* ws_o;
     float* ws_ml;
+    int32_t* ws_count;  // split-K arrival counters [B][Hkv] (nullable: merge in a separate kernel)
     int32_t* err;
     int32_t Hq, Hkv, bs, max_blocks, num_blocks, max_slots, split_tokens, max_splits;
     int32_t tab_cap;  // block-table entries the shared table holds (even)
@@ -543,6 +544,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     __syncthreads();
 
     // ---- merge the warps and write ---------------------------------------------
+    if (SPLIT && ctx == 0) {
+        // no tokens: a zero row (no partials, no counter)
+        for (int e = tid; e < G * D; e += kThreads)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G) * D + e] = __float2bfloat16_rn(0.f);
+        return;
+    }
     for (int e = tid; e < G * D; e += kThreads) {
         const int h = e / D, dim = e % D;
         float mm = -1e30f;
@@ -567,6 +574,35 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             const float r = L > 0.f ? O / L : 0.f;
             reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(r);
         }
+    }
+    if (SPLIT && p.ws_count) {
+        // Fused split-K merge: the last split of (b, kv head) to finish merges
+        // all of them (partials are read from L2, past this SM's L1).
+        __shared__ int s_last;
+        const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
+        int32_t* cnt = p.ws_count + size_t(b) * p.Hkv + kvh;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(cnt, 1) == ns - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        for (int e = tid; e < G * D; e += kThreads) {
+            const int h = e / D, dim = e % D;
+            const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
+            const float* ml = p.ws_ml + hrow * p.max_splits * 2;
+            const float* o = p.ws_o + hrow * p.max_splits * D + dim;
+            float mm = -1e30f;
+            for (int q = 0; q < ns; ++q) mm = fmaxf(mm, __ldcg(ml + 2 * q));
+            float L = 0.f, O = 0.f;
+            for (int q = 0; q < ns; ++q) {
+                const float c = fast_exp2(__ldcg(ml + 2 * q) - mm);
+                L += c * __ldcg(ml + 2 * q + 1);
+                O += c * __ldcg(o + size_t(q) * D);
+            }
+            reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        }
+        if (tid == 0) *cnt = 0;  // ready for the next call
     }
 }
 

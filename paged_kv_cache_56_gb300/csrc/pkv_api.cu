@@ -161,30 +161,44 @@ static int check_desc(const pkv_cache_desc* c) {
 
 static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
-template <int D, int G, bool INT8, bool SPLIT>
-static int launch_decode_t(const DecodeParams& p, dim3 grid, size_t smem, cudaStream_t st) {
-    auto fn = decode_kernel<D, G, INT8, SPLIT>;
-    static int configured[64] = {0};  // per device: largest dynamic smem set so far
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-    if (int(smem) > configured[dev]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured[dev] = int(smem);
-    }
-    fn<<<grid, kThreads, smem, st>>>(p);
-    return cuda_status(cudaGetLastError());
-}
+using DecodeFn = void (*)(DecodeParams);
 
 template <int D, bool INT8, bool SPLIT>
-static int dispatch_g(int g, const DecodeParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+static DecodeFn pick_g(int g) {
     switch (g) {
-        case 1: return launch_decode_t<D, 1, INT8, SPLIT>(p, grid, smem, st);
-        case 2: return launch_decode_t<D, 2, INT8, SPLIT>(p, grid, smem, st);
-        case 4: return launch_decode_t<D, 4, INT8, SPLIT>(p, grid, smem, st);
-        case 8: return launch_decode_t<D, 8, INT8, SPLIT>(p, grid, smem, st);
-        default: return PKV_ERR_UNSUPPORTED;
+        case 1: return decode_kernel<D, 1, INT8, SPLIT>;
+        case 2: return decode_kernel<D, 2, INT8, SPLIT>;
+        case 4: return decode_kernel<D, 4, INT8, SPLIT>;
+        case 8: return decode_kernel<D, 8, INT8, SPLIT>;
+        default: return nullptr;
     }
+}
+
+// The decode instantiation for a shape, and a small index for per-kernel state.
+static DecodeFn pick_decode(int d, int g, bool int8, bool split, int* index) {
+    const int lg = g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3;
+    *index = (((d == 128) * 4 + lg) * 2 + int8) * 2 + split;
+    if (d == 128) {
+        if (int8) return split ? pick_g<128, true, true>(g) : pick_g<128, true, false>(g);
+        return split ? pick_g<128, false, true>(g) : pick_g<128, false, false>(g);
+    }
+    if (int8) return split ? pick_g<64, true, true>(g) : pick_g<64, true, false>(g);
+    return split ? pick_g<64, false, true>(g) : pick_g<64, false, false>(g);
+}
+
+// Raises the kernel's dynamic shared-memory limit (once per kernel, device
+// and size) so that it can be launched or sized with `smem` bytes.
+static int allow_smem(DecodeFn fn, int index, size_t smem) {
+    static int configured[32][64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+    if (int(smem) > configured[index][dev]) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured[index][dev] = int(smem);
+    }
+    return PKV_OK;
 }
 
 static size_t decode_smem(int d, int g, bool int8, int tab_cap) {
@@ -305,10 +319,33 @@ int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_
     return launch_reduce(ws_o, ws_ml, ctx_lens, B, Hq, head_dim, split_tokens, max_splits, out, nullptr, stream);
 }
 
+static int decode_tab_cap(const pkv_cache_desc* c, int32_t split_tokens, int32_t max_blocks) {
+    int tab_cap = split_tokens > 0 ? split_tokens / c->block_size : max_blocks;
+    return tab_cap + (tab_cap & 1);
+}
+
+int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_t max_blocks) {
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (split_tokens < 0 || max_blocks <= 0) return PKV_ERR_INVALID;
+    if (split_tokens > 0 && (split_tokens % c->block_size || split_tokens % kTile)) return PKV_ERR_INVALID;
+    const bool int8 = c->dtype == PKV_DTYPE_INT8;
+    const int g = c->num_q_heads / c->num_kv_heads;
+    const size_t smem = decode_smem(c->head_dim, g, int8, decode_tab_cap(c, split_tokens, max_blocks));
+    if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
+    int index = 0;
+    DecodeFn fn = pick_decode(c->head_dim, g, int8, split_tokens > 0, &index);
+    if (!fn) return PKV_ERR_UNSUPPORTED;
+    if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) return PKV_ERR_CUDA;
+    return n;
+}
+
 int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables, int32_t max_blocks,
                          const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
-                         int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, void* out,
-                         void* stream) {
+                         int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count,
+                         void* out, void* stream) {
     int st = check_desc(c);
     if (st != PKV_OK) return st;
     if (B < 0 || max_blocks <= 0 || split_tokens < 0 || !(sm_scale == sm_scale)) return PKV_ERR_INVALID;
@@ -325,9 +362,9 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
         if (int64_t(max_splits) * split_tokens < max_ctx || max_splits > 65535) return PKV_ERR_INVALID;
         if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
     }
+    if (split && ws_count && (reinterpret_cast<uintptr_t>(ws_count) & 3u)) return PKV_ERR_INVALID;
     const int g = c->num_q_heads / c->num_kv_heads;
-    int tab_cap = split ? split_tokens / c->block_size : max_blocks;
-    tab_cap += tab_cap & 1;
+    const int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
     const size_t smem = decode_smem(c->head_dim, g, int8, tab_cap);
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
@@ -344,6 +381,7 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     p.out = static_cast<uint16_t*>(out);
     p.ws_o = ws_o;
     p.ws_ml = ws_ml;
+    p.ws_count = split ? ws_count : nullptr;
     p.err = c->err_word;
     p.Hq = c->num_q_heads;
     p.Hkv = c->num_kv_heads;
@@ -358,15 +396,13 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
 
     const dim3 grid(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
     auto s = static_cast<cudaStream_t>(stream);
-    int rc;
-    if (c->head_dim == 128) {
-        if (int8) rc = split ? dispatch_g<128, true, true>(g, p, grid, smem, s) : dispatch_g<128, true, false>(g, p, grid, smem, s);
-        else rc = split ? dispatch_g<128, false, true>(g, p, grid, smem, s) : dispatch_g<128, false, false>(g, p, grid, smem, s);
-    } else {
-        if (int8) rc = split ? dispatch_g<64, true, true>(g, p, grid, smem, s) : dispatch_g<64, true, false>(g, p, grid, smem, s);
-        else rc = split ? dispatch_g<64, false, true>(g, p, grid, smem, s) : dispatch_g<64, false, false>(g, p, grid, smem, s);
-    }
-    if (rc != PKV_OK || !split) return rc;
+    int index = 0;
+    DecodeFn fn = pick_decode(c->head_dim, g, int8, split, &index);
+    if (!fn) return PKV_ERR_UNSUPPORTED;
+    if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
+    fn<<<grid, kThreads, smem, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (!split || ws_count) return PKV_OK;
     return launch_reduce(ws_o, ws_ml, ctx_lens, B, c->num_q_heads, c->head_dim, split_tokens, max_splits, out,
                          c->err_word, stream);
 }

@@ -45,7 +45,7 @@ EXPORTED = (
     "pkv_attach_shared", "pkv_num_free", "pkv_request_table", "pkv_free_list",
     "pkv_build_block_tables", "pkv_append_kv", "pkv_quantize_full_blocks",
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
-    "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes",
+    "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
 )
 
 
@@ -97,7 +97,8 @@ def lib() -> ctypes.CDLL:
             "pkv_quantize_full_blocks": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP]),
             "pkv_quantize_blocks_from": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _VP, _I32, _VP]),
             "pkv_decode_attention": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP, _I32,
-                                                    ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP]),
+                                                    ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
+            "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
             "pkv_splitk_reduce": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP]),
             "pkv_splitk_ws_o_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
             "pkv_splitk_ws_ml_bytes": (ctypes.c_size_t, [_I32, _I32, _I32]),
@@ -270,10 +271,17 @@ def pkv_splitk_ws_ml_bytes(B: int, Hq: int, max_splits: int) -> int:
     return lib().pkv_splitk_ws_ml_bytes(B, Hq, max_splits)
 
 
+def pkv_decode_ctas_per_sm(desc: CacheDesc, split_tokens: int, max_blocks: int) -> int:
+    n = lib().pkv_decode_ctas_per_sm(_desc_ptr(desc), split_tokens, max_blocks)
+    if n < 0:
+        raise PkvError("pkv_decode_ctas_per_sm", n)
+    return n
+
+
 def pkv_decode_attention(desc: CacheDesc, q: torch.Tensor, block_tables: torch.Tensor,
                          ctx_lens: torch.Tensor, slots, sm_scale: float, out: torch.Tensor,
                          split_tokens: int = 0, max_splits: int = 0, ws_o=None, ws_ml=None,
-                         stream=None) -> None:
+                         ws_count=None, stream=None) -> None:
     B = ctx_lens.numel()
     max_blocks = block_tables.shape[-1] if block_tables.dim() == 2 else 0
     hq, d = desc.num_q_heads, desc.head_dim
@@ -282,13 +290,14 @@ def pkv_decode_attention(desc: CacheDesc, q: torch.Tensor, block_tables: torch.T
     tp = _dev(block_tables, "block_tables", torch.int32, B * max_blocks)
     cp = _dev(ctx_lens, "ctx_lens", torch.int32, B)
     sp = _opt_dev(slots, "slots", torch.int32, B)
-    wo = wml = None
+    wo = wml = wc = None
     if split_tokens > 0:
         wo = _dev(ws_o, "ws_o", torch.float32, B * hq * max_splits * d)
         wml = _dev(ws_ml, "ws_ml", torch.float32, B * hq * max_splits * 2)
+        wc = _opt_dev(ws_count, "ws_count", torch.int32, B * desc.num_kv_heads)
     _check("pkv_decode_attention",
            lib().pkv_decode_attention(_desc_ptr(desc), qp, tp, max_blocks, cp, sp, B, float(sm_scale),
-                                      split_tokens, max_splits, wo, wml, outp, _stream(stream)))
+                                      split_tokens, max_splits, wo, wml, wc, outp, _stream(stream)))
 
 
 def pkv_splitk_reduce(ws_o: torch.Tensor, ws_ml: torch.Tensor, ctx_lens: torch.Tensor, num_q_heads: int,

@@ -58,19 +58,38 @@ class LayerCache:
 
 
 def choose_split_tokens(batch: int, num_kv_heads: int, max_ctx: int, block_size: int,
-                        num_sms: int, ctas_per_sm: int = 3) -> int:
-    """Split length (a multiple of 16 and of block_size) that gives about
-    num_sms * ctas_per_sm CTAs for the longest context, or 0 when one CTA per
-    (sequence, kv head) already fills the GPU."""
+                        num_sms: int, ctas_per_sm: int) -> int:
+    """Split length (a multiple of 16 and of block_size) such that the
+    (sequence, kv head, split) CTAs of the longest context fit in one wave of
+    num_sms * ctas_per_sm resident CTAs; 0 (no split) when one CTA per
+    (sequence, kv head) already fills a wave."""
     pairs = batch * num_kv_heads
-    target = num_sms * ctas_per_sm
-    if pairs >= target or max_ctx <= 0:
+    slots = num_sms * ctas_per_sm
+    splits = slots // max(pairs, 1)
+    if splits <= 1 or max_ctx <= 0:
         return 0
-    splits = max(1, -(-target // pairs))
     unit = max(16, block_size)
     tok = -(-max_ctx // splits)
-    tok = -(-tok // unit) * unit
-    return max(unit, tok)
+    return max(unit, -(-tok // unit) * unit)
+
+
+def plan_split_tokens(cache: "PagedKVCache", batch: int, max_ctx: int, num_sms: int | None = None) -> int:
+    """choose_split_tokens with this cache's measured decode occupancy."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.device(cache.device)).multi_processor_count
+    desc = cache.layers[0].desc
+    unit = max(16, cache.bs)
+    occ = pkv.pkv_decode_ctas_per_sm(desc, unit, cache.max_blocks)
+    split = choose_split_tokens(batch, cache.hkv, max_ctx, cache.bs, num_sms, occ)
+    if split:
+        occ2 = pkv.pkv_decode_ctas_per_sm(desc, split, cache.max_blocks)
+        if occ2 < occ:
+            split = choose_split_tokens(batch, cache.hkv, max_ctx, cache.bs, num_sms, occ2)
+    else:
+        occ0 = pkv.pkv_decode_ctas_per_sm(desc, 0, cache.max_blocks)
+        if batch * cache.hkv < num_sms * occ0:
+            split = choose_split_tokens(batch, cache.hkv, max_ctx, cache.bs, num_sms, occ0)
+    return split
 
 
 @dataclass
@@ -238,7 +257,7 @@ class StepBuffers:
     """Device-side control arrays (and split-K workspace) of decode steps for
     up to max_batch sequences; pinned host mirrors make the uploads async."""
 
-    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int = 0):
+    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int = 0, fused_merge: bool = True):
         dev = cache.device
         self.cache = cache
         self.max_batch = max_batch
@@ -258,8 +277,11 @@ class StepBuffers:
         if split_tokens:
             self.ws_o = torch.empty(max_batch * cache.hq * self.max_splits * cache.d, dtype=torch.float32, device=dev)
             self.ws_ml = torch.empty(max_batch * cache.hq * self.max_splits * 2, dtype=torch.float32, device=dev)
+            # arrival counters of the fused split-K merge (kept at zero between calls)
+            self.ws_count = (torch.zeros(max_batch * cache.hkv, dtype=torch.int32, device=dev)
+                             if fused_merge else None)
         else:
-            self.ws_o = self.ws_ml = None
+            self.ws_o = self.ws_ml = self.ws_count = None
         self.B = 0
         self.copied = torch.cuda.Event()  # the last upload's copies have run
         self.copied.record()
@@ -298,7 +320,7 @@ def run_layers(cache: PagedKVCache, bufs: StepBuffers, q, k_new, v_new, out, sm_
         if cache.int8 and (quantize == "always" or (plan is not None and (plan.fill_blocks >= 0).any())):
             pkv.pkv_quantize_full_blocks(lc.desc, bufs.fill[:B], bufs.slot[:B], stream)
         pkv.pkv_decode_attention(lc.desc, q[li], bufs.tab[:B], bufs.ctx[:B], bufs.slot[:B], sm_scale, out[li],
-                                 bufs.split_tokens, bufs.max_splits, bufs.ws_o, bufs.ws_ml, stream)
+                                 bufs.split_tokens, bufs.max_splits, bufs.ws_o, bufs.ws_ml, bufs.ws_count, stream)
 
 
 def decode_step(cache: PagedKVCache, bufs: StepBuffers, req_ids, q, k_new, v_new, out, sm_scale: float,
@@ -339,7 +361,7 @@ class GraphStep:
         self.attn_graph = None
 
     def launches_per_step(self) -> int:
-        per_attn = 2 if self.bufs.split_tokens else 1
+        per_attn = 2 if (self.bufs.split_tokens and self.bufs.ws_count is None) else 1
         return self.cache.L * (1 + (1 if self.cache.int8 else 0) + self.R * per_attn)
 
     def _layers(self, attention_only: bool = False) -> None:
@@ -353,7 +375,7 @@ class GraphStep:
             for r in range(self.R):
                 qi = li * self.R + r
                 pkv.pkv_decode_attention(lc.desc, self.q[qi], b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
-                                         self.out[qi], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml)
+                                         self.out[qi], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
 
     def run_eager(self) -> None:
         self._layers()

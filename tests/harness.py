@@ -16,7 +16,8 @@ import torch
 from oracle.attention import decode_attention
 from oracle.cache import SequenceHistory
 from paged_kv_cache_56_gb300 import synth
-from paged_kv_cache_56_gb300.runtime import PagedKVCache, StepBuffers, decode_step, prefill
+from paged_kv_cache_56_gb300.runtime import (GraphStep, PagedKVCache, StepBuffers, decode_step,
+                                              plan_split_tokens, prefill)
 
 ATOL, RTOL = 2e-3, 1e-2  # |gpu - ref| <= ATOL + RTOL * |ref| on bf16 outputs
 
@@ -38,7 +39,7 @@ class Workload:
     def __init__(self, seed: int, num_layers: int, prior, Hq: int, Hkv: int, d: int, bs: int,
                  num_blocks: int, int8: bool, split_tokens: int = 0, max_blocks: int | None = None,
                  head_scale: bool = False, outliers: bool = False, shuffle: bool = True,
-                 req_ids=None, device="cuda", layers_with_data=None):
+                 req_ids=None, device="cuda", fused_merge: bool = True, graph: bool = False, repeat: int = 1):
         self.seed, self.L, self.prior = seed, num_layers, list(prior)
         self.Hq, self.Hkv, self.d, self.bs = Hq, Hkv, d, bs
         self.int8 = int8
@@ -51,8 +52,14 @@ class Workload:
         order = synth.permutation(seed, num_blocks) if shuffle else None
         self.cache = PagedKVCache(num_layers, num_blocks, Hq, Hkv, d, bs, int8, max_slots=self.B,
                                   max_blocks_per_seq=self.max_blocks, device=device, initial_order=order)
-        self.bufs = StepBuffers(self.cache, self.B, split_tokens)
+        if split_tokens == "auto":  # as the benchmark sizes it: one wave of CTAs
+            split_tokens = plan_split_tokens(self.cache, self.B, self.max_blocks * bs)
+        self.split_tokens = split_tokens
+        self.bufs = StepBuffers(self.cache, self.B, split_tokens, fused_merge=fused_merge)
         self.step_no = 0
+        self.graph = graph
+        self.R = repeat
+        self.gs = None
         for r, n in zip(self.req_ids, self.prior):
             self.cache.add_sequence(r, -(-n // bs))
         for li in range(num_layers):
@@ -83,18 +90,47 @@ class Workload:
                             device=device or self.device)
 
     # -- GPU ------------------------------------------------------------------
+    def q_for(self, qi, step, reqs, device=None):
+        """Query of attention call qi (= layer * R + repeat) at decode step ``step``.
+        Repeat r > 0 of a layer draws its own query stream."""
+        layer, rep = divmod(qi, self.R)
+        if rep == 0:
+            return self.q(layer, step, reqs, device)
+        return synth.q_rows(self.seed, 1000 * (rep + 1) + layer, step, reqs, self.Hq, self.d,
+                            mult=self.q_mult(layer), device=device or self.device)
+
     def step(self):
-        """One decode step through the C ABI; returns out [L, B, Hq, d] (device bf16)."""
+        """One decode step through the C ABI; returns out [L*R, B, Hq, d] (device bf16).
+        With graph=True the step runs as the bench runs it: one eager step, then
+        replays of the captured CUDA graph."""
         t = self.step_no
         lens = [self.cache.seqs[r].length for r in self.req_ids]
         pos = torch.tensor(lens, dtype=torch.int64)
-        q = [self.q(li, t, self.req_ids) for li in range(self.L)]
-        kn = [self.kv(li, synth.KIND_K, self.req_ids, pos) for li in range(self.L)]
-        vn = [self.kv(li, synth.KIND_V, self.req_ids, pos) for li in range(self.L)]
-        out = torch.empty((self.L, self.B, self.Hq, self.d), dtype=torch.bfloat16, device=self.device)
-        decode_step(self.cache, self.bufs, self.req_ids, q, kn, vn, list(out), self.sm_scale)
+        q = torch.stack([self.q_for(qi, t, self.req_ids) for qi in range(self.L * self.R)])
+        kn = torch.stack([self.kv(li, synth.KIND_K, self.req_ids, pos) for li in range(self.L)])
+        vn = torch.stack([self.kv(li, synth.KIND_V, self.req_ids, pos) for li in range(self.L)])
+        if not self.graph and self.R == 1:
+            out = torch.empty((self.L, self.B, self.Hq, self.d), dtype=torch.bfloat16, device=self.device)
+            decode_step(self.cache, self.bufs, self.req_ids, list(q), list(kn), list(vn), list(out), self.sm_scale)
+            self.step_no += 1
+            return out
+        plan = self.cache.plan_step(self.req_ids)
+        self.bufs.upload(plan)
+        first = self.gs is None
+        if first:
+            self.gs = GraphStep(self.cache, self.bufs, self.sm_scale, self.R)
+        self.gs.q.copy_(q)
+        self.gs.k.copy_(kn)
+        self.gs.v.copy_(vn)
+        if first or not self.graph:
+            self.gs.run_eager()
+            if self.graph:
+                self.gs.capture()
+        else:
+            self.gs.replay()
+        self.cache.commit_step(self.req_ids)
         self.step_no += 1
-        return out
+        return self.gs.out.clone()
 
     def error_bits(self) -> int:
         return sum(lc.error_bits() for lc in self.cache.layers)
@@ -108,13 +144,27 @@ class Workload:
                  self.kv(layer, synth.KIND_V, r, pos, "cpu").float().numpy())
         return h
 
-    def oracle_out(self, layer: int, i: int, step: int, heads=None) -> np.ndarray:
-        """Oracle output [Hq, d] of sequence i at decode step ``step``."""
+    def oracle_out(self, layer: int, i: int, step: int, rep: int = 0, hist=None) -> np.ndarray:
+        """Oracle output [Hq, d] of sequence i at decode step ``step`` (attention
+        call ``layer * R + rep``)."""
         n = self.prior[i] + step + 1
-        h = self.history(layer, i, n)
+        h = hist if hist is not None else self.history(layer, i, n)
         k, v = h.context()
-        q = self.q(layer, step, [self.req_ids[i]], "cpu")[0].float().numpy()
+        q = self.q_for(layer * self.R + rep, step, [self.req_ids[i]], "cpu")[0].float().numpy()
         return decode_attention(q, k, v, self.sm_scale)
+
+    def oracle_steps(self, layer: int, i: int, steps: int, rep: int = 0) -> list:
+        """Oracle outputs of sequence i for decode steps 0..steps-1, growing one
+        history a token at a time (quantizing at its own fill points)."""
+        h = self.history(layer, i, self.prior[i])
+        r = self.req_ids[i]
+        outs = []
+        for t in range(steps):
+            p = torch.tensor([self.prior[i] + t])
+            h.append(self.kv(layer, synth.KIND_K, r, p, "cpu").float().numpy(),
+                     self.kv(layer, synth.KIND_V, r, p, "cpu").float().numpy())
+            outs.append(self.oracle_out(layer, i, t, rep, hist=h))
+        return outs
 
     def check_pool_bytes(self, layer: int, i: int, n: int) -> int:
         """Compares the pools of sequence i (first n tokens) with the oracle's
@@ -123,17 +173,18 @@ class Workload:
         lc = self.cache.layers[layer]
         tab = self.cache.table(self.req_ids[i])
         nf = n // self.bs
+        nb = -(-n // self.bs)
+        ids = torch.tensor(tab[: (nf if self.int8 else nb)], dtype=torch.long, device=lc.k_pool.device)
         if self.int8:
-            kp = lc.k_pool.cpu().numpy()
-            vp = lc.v_pool.cpu().numpy()
-            sc = lc.scales.cpu().numpy()
+            kp = lc.k_pool[ids].cpu().numpy()
+            vp = lc.v_pool[ids].cpu().numpy()
+            sc = lc.scales[ids].cpu().numpy()
             for bi in range(nf):
                 qk, sk, qv, sv = h.blocks[bi]
-                pb = tab[bi]
-                assert np.array_equal(kp[pb], qk), (layer, i, bi, "K codes")
-                assert np.array_equal(vp[pb], qv), (layer, i, bi, "V codes")
-                assert np.array_equal(sc[pb, :, 0].view(np.uint32), sk.view(np.uint32)), (layer, i, bi, "K scale")
-                assert np.array_equal(sc[pb, :, 1].view(np.uint32), sv.view(np.uint32)), (layer, i, bi, "V scale")
+                assert np.array_equal(kp[bi], qk), (layer, i, bi, "K codes")
+                assert np.array_equal(vp[bi], qv), (layer, i, bi, "V codes")
+                assert np.array_equal(sc[bi, :, 0].view(np.uint32), sk.view(np.uint32)), (layer, i, bi, "K scale")
+                assert np.array_equal(sc[bi, :, 1].view(np.uint32), sv.view(np.uint32)), (layer, i, bi, "V scale")
             rem = n - nf * self.bs
             if rem:
                 slot = self.cache.seqs[self.req_ids[i]].slot
@@ -143,12 +194,11 @@ class Workload:
                 vt = lc.v_tail[slot, :, :rem].float().cpu().numpy()
                 assert np.array_equal(vt, vr[nf * self.bs:].transpose(1, 0, 2)), (layer, i, "V tail")
             return nf
-        kp = lc.k_pool.float().cpu().numpy()
-        vp = lc.v_pool.float().cpu().numpy()
+        kp = lc.k_pool[ids].float().cpu().numpy()
+        vp = lc.v_pool[ids].float().cpu().numpy()
         kr, vr = h.raw()
-        for bi in range(-(-n // self.bs)):
+        for bi in range(nb):
             lo, hi = bi * self.bs, min(n, (bi + 1) * self.bs)
-            pb = tab[bi]
-            assert np.array_equal(kp[pb][:, : hi - lo], kr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "K rows")
-            assert np.array_equal(vp[pb][:, : hi - lo], vr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "V rows")
-        return -(-n // self.bs)
+            assert np.array_equal(kp[bi][:, : hi - lo], kr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "K rows")
+            assert np.array_equal(vp[bi][:, : hi - lo], vr[lo:hi].transpose(1, 0, 2)), (layer, i, bi, "V rows")
+        return nb

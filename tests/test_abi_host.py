@@ -59,7 +59,7 @@ def _desc(**kw):
 ])
 def test_descriptor_validation(L, kw, code):
     d = _desc(**kw)
-    rc = L.pkv_decode_attention(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None)
+    rc = L.pkv_decode_attention(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, None, 16, None)
     assert rc == code
     rc = L.pkv_append_kv(ctypes.byref(d), 16, 16, 16, 16, 16, 1, None)
     assert rc == code
@@ -68,15 +68,19 @@ def test_descriptor_validation(L, kw, code):
 def test_argument_validation(L):
     d = _desc()
     attn = L.pkv_decode_attention
-    assert attn(None, 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
-    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 0, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_OK  # B = 0
-    assert attn(ctypes.byref(d), None, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
-    assert attn(ctypes.byref(d), 16, 16, 0, 16, 16, 1, 0.1, 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
-    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, float("nan"), 0, 0, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(None, 16, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 0, 0.1, 0, 0, None, None, None, 16, None) == pkv.PKV_OK  # B = 0
+    assert attn(ctypes.byref(d), None, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 0, 16, 16, 1, 0.1, 0, 0, None, None, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, float("nan"), 0, 0, None, None, None, 16, None) == pkv.PKV_ERR_INVALID
     # split must be a multiple of block size and of 16; max_splits must cover max_blocks * bs
-    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 24, 8, 16, 16, 16, None) == pkv.PKV_ERR_INVALID
-    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 1, 16, 16, 16, None) == pkv.PKV_ERR_INVALID
-    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 2, None, 16, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 24, 8, 16, 16, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 1, 16, 16, None, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 2, None, 16, None, 16, None) == pkv.PKV_ERR_INVALID
+    # misaligned split-K arrival counters
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, 32, 2, 16, 16, 18, 16, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_decode_ctas_per_sm(ctypes.byref(_desc(head_dim=80)), 0, 4) == pkv.PKV_ERR_UNSUPPORTED
+    assert L.pkv_decode_ctas_per_sm(ctypes.byref(d), 24, 4) == pkv.PKV_ERR_INVALID
     assert L.pkv_append_kv(ctypes.byref(d), 16, 16, 16, 16, 16, 0, None) == pkv.PKV_OK  # T = 0
     assert L.pkv_append_kv(ctypes.byref(d), 16, 16, None, 16, 16, 3, None) == pkv.PKV_ERR_INVALID
     assert L.pkv_quantize_full_blocks(ctypes.byref(d), 16, 16, 1, None) == pkv.PKV_ERR_INVALID  # BF16 cache

@@ -53,3 +53,28 @@ def test_split_counts_agree(int8):
         res[split] = w.step().float().cpu().numpy()
     for split in (16, 48, 112):
         assert_close(res[split], res[0], f"split {split} vs none")
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_fused_and_separate_merge_agree(int8):
+    res = {}
+    for fused in (True, False):
+        w = Workload(seed=9, prior=(100, 3, 77, 111), int8=int8, split_tokens=32, max_blocks=8, fused_merge=fused,
+                     **TINY)
+        res[fused] = torch.stack([w.step() for _ in range(5)]).cpu()
+        assert w.error_bits() == 0
+        if fused:
+            assert int(w.bufs.ws_count.abs().sum()) == 0  # counters are left at zero
+    assert torch.equal(res[True], res[False])
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_graph_replay_matches_oracle(int8):
+    w = Workload(seed=21, prior=(5, 40, 16, 63), int8=int8, split_tokens=32, max_blocks=9, graph=True, repeat=2,
+                 **TINY)
+    for t in range(20):
+        out = w.step().float().cpu().numpy()
+        for i in range(w.B):
+            for rep in range(2):
+                assert_close(out[rep, i], w.oracle_out(0, i, t, rep), f"step {t} seq {i} rep {rep}")
+    assert w.error_bits() == 0
