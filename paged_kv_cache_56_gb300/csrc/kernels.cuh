@@ -23,6 +23,13 @@
 
 #include "ptx.cuh"
 
+#ifndef PKV_STAGES_INT8
+#define PKV_STAGES_INT8 3  // bulk-copy stages per warp, INT8 cache (4 KB each at d = 128)
+#endif
+#ifndef PKV_STAGES_BF16
+#define PKV_STAGES_BF16 2  // bulk-copy stages per warp, bf16 cache (8 KB each at d = 128)
+#endif
+
 namespace pkv {
 
 constexpr int kWarps = 4;
@@ -66,7 +73,7 @@ struct DecodeTraits {
     static constexpr int kRowBytes = D * kElemBytes;
     static constexpr int kTileBytes = kTile * kRowBytes;  // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = INT8 ? 4 : 3;
+    static constexpr int kStages = INT8 ? PKV_STAGES_INT8 : PKV_STAGES_BF16;
 };
 
 // Shared-memory bytes of a decode CTA before its block table.
@@ -212,9 +219,10 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
                                          WarpState<D>& st) {
     using Gm = Geom<D, I8>;
     constexpr bool F16 = I8;
-    // ---- S = K . Q^T
+    // ---- S = K . Q^T (two independent accumulator chains, summed)
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     {
+        float s2[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t k0[Gm::kKW], k1[Gm::kKW];
         load_run<Gm::kKB>(K, g, t * Gm::kKB, k0);
         load_run<Gm::kKB>(K, g + 8, t * Gm::kKB, k1);
@@ -228,8 +236,11 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
                 a0 = k0[2 * ks]; a2 = k0[2 * ks + 1];
                 a1 = k1[2 * ks]; a3 = k1[2 * ks + 1];
             }
-            mma16816<F16>(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            if (ks & 1) mma16816<F16>(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else mma16816<F16>(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] += s2[i];
     }
     const float f0 = ksc * hs[0], f1 = ksc * hs[1];
     s[0] *= f0; s[1] *= f1; s[2] *= f0; s[3] *= f1;
@@ -345,14 +356,15 @@ __device__ __forceinline__ int load_q_frags(const uint16_t* qrow, int g, int t, 
     return e;
 }
 
-// Waits for an mbarrier phase for at most ~1 s of GPU time.
+// Waits for an mbarrier phase for at most ~1 s of GPU time. A waiting warp
+// sleeps in try_wait (up to 2 us per poll) rather than spinning, so it does
+// not take issue slots from warps that have data.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
         uint64_t t;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
         if (t - t0 > 1000000000ull) return false;
@@ -587,18 +599,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         __syncthreads();
         if (!s_last) return;
         __threadfence();
+        // Online merge of the splits' states, 16 splits per batch of
+        // independent loads (partials are read from L2, past this SM's L1).
         for (int e = tid; e < G * D; e += kThreads) {
             const int h = e / D, dim = e % D;
             const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
-            const float* ml = p.ws_ml + hrow * p.max_splits * 2;
+            const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + hrow * p.max_splits * 2);
             const float* o = p.ws_o + hrow * p.max_splits * D + dim;
-            float mm = -1e30f;
-            for (int q = 0; q < ns; ++q) mm = fmaxf(mm, __ldcg(ml + 2 * q));
-            float L = 0.f, O = 0.f;
-            for (int q = 0; q < ns; ++q) {
-                const float c = fast_exp2(__ldcg(ml + 2 * q) - mm);
-                L += c * __ldcg(ml + 2 * q + 1);
-                O += c * __ldcg(o + size_t(q) * D);
+            float mm = -1e30f, L = 0.f, O = 0.f;
+            for (int q0 = 0; q0 < ns; q0 += 16) {
+                float2 v[16];
+                float ov[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (q0 + u < ns) {
+                        v[u] = __ldcg(ml + q0 + u);
+                        ov[u] = __ldcg(o + size_t(q0 + u) * D);
+                    } else {
+                        v[u] = make_float2(-1e30f, 0.f);
+                        ov[u] = 0.f;
+                    }
+                }
+                float bm = mm;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) bm = fmaxf(bm, v[u].x);
+                const float c = fast_exp2(mm - bm);
+                L *= c;
+                O *= c;
+                mm = bm;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float w = fast_exp2(v[u].x - mm);
+                    L += w * v[u].y;
+                    O += w * ov[u];
+                }
             }
             reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
         }
@@ -647,6 +681,7 @@ __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restr
     const float* o = ws_o + hrow * max_splits * D;
     for (int dim = tid; dim < D; dim += 128) {
         float acc = 0.f;
+#pragma unroll 8
         for (int s = 0; s < ns; ++s) acc += cw[s] * o[size_t(s) * D + dim];
         reinterpret_cast<__nv_bfloat16*>(out)[hrow * D + dim] = __float2bfloat16_rn(acc * inv);
     }

@@ -381,7 +381,8 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     p.out = static_cast<uint16_t*>(out);
     p.ws_o = ws_o;
     p.ws_ml = ws_ml;
-    p.ws_count = split ? ws_count : nullptr;
+    const bool fuse = split && ws_count;
+    p.ws_count = fuse ? ws_count : nullptr;
     p.err = c->err_word;
     p.Hq = c->num_q_heads;
     p.Hkv = c->num_kv_heads;
@@ -402,7 +403,7 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
     fn<<<grid, kThreads, smem, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-    if (!split || ws_count) return PKV_OK;
+    if (!split || fuse) return PKV_OK;
     return launch_reduce(ws_o, ws_ml, ctx_lens, B, c->num_q_heads, c->head_dim, split_tokens, max_splits, out,
                          c->err_word, stream);
 }

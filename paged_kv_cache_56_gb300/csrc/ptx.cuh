@@ -51,12 +51,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: returns false if the phase did not complete within max_iters
-// polls (each try_wait may itself suspend the thread for a short while).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t max_iters) {
-    for (uint32_t i = 0; i < max_iters; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+// Like mbar_try_wait, but lets the hardware suspend the thread for up to
+// `ns` nanoseconds while the phase is incomplete instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
 }
 
 // ---- bulk asynchronous copy global -> shared (no tensor map) ----------------
