@@ -52,6 +52,7 @@ extern "C" {
 #define PKV_ERR_EXISTS        -4  /* request id is already live */
 #define PKV_ERR_UNSUPPORTED   -5  /* shape outside the compiled set (see below) */
 #define PKV_ERR_CUDA          -6  /* a CUDA runtime call failed */
+#define PKV_ERR_TOO_LARGE     -7  /* the request needs more than the library's fixed scratch array */
 
 /* bits a kernel ORs into the descriptor's error word */
 #define PKV_DEVERR_BLOCK_ID    1  /* block id < 0 or >= num_blocks */
@@ -228,6 +229,40 @@ int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_
 
 size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits);
 size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
+
+/* Bytes of the library-owned split-K scratch array used by
+ * pkv_decode_attention_static_ws (8 MiB, held on every GPU that loads the
+ * library for the life of the process). */
+#define PKV_STATIC_WS_BYTES (8u << 20)
+
+/* pkv_decode_attention without a caller-provided workspace: the pages have
+ * no counterpart; this exists for callers that cannot allocate device memory
+ * when they decode -- an engine that gives all free HBM to its cache pool at
+ * start-up and forbids later allocations, code running inside such an
+ * engine, or a latency-critical loop that must not pay for cudaMalloc's
+ * implicit synchronisation. The split-K partials and the merge's arrival
+ * counters live in a fixed array inside the library; this function allocates
+ * nothing and calls no allocating routine.
+ *
+ * Arguments and results are those of pkv_decode_attention with split_tokens
+ * and max_splits as given (split_tokens == 0 uses no scratch at all). The
+ * scratch needed is B*Hkv*4 bytes of counters plus
+ * pkv_splitk_ws_ml_bytes(B, Hq, max_splits) and
+ * pkv_splitk_ws_o_bytes(B, Hq, d, max_splits), each part rounded up to
+ * 256 bytes; if that exceeds PKV_STATIC_WS_BYTES the call returns
+ * PKV_ERR_TOO_LARGE and launches nothing.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the current one); make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents: each call first clears its counters (an asynchronous memset on
+ * the stream), then writes its partials before reading them. Calls whose
+ * executions overlap on the GPU -- on different streams, or from different
+ * host threads -- race on the array and give wrong results; serialise them. */
+int pkv_decode_attention_static_ws(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
+                                   int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
+                                   void* out, void* stream);
 
 #ifdef __cplusplus
 }

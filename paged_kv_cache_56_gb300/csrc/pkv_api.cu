@@ -409,3 +409,68 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention with library-owned split-K scratch (no allocation).
+//
+// Some callers cannot allocate device memory at decode time: an engine that
+// hands all free HBM to its KV-cache pool at start-up and forbids later
+// allocations (a cudaMalloc would fail or evict cache), a plugin living
+// inside such an engine, or a latency-critical loop that must not pay for
+// cudaMalloc's implicit synchronisation. This entry point takes no workspace
+// argument: the split-K partials and arrival counters live in the fixed
+// array below, which every GPU that loads the library holds until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace pkv {
+static __device__ __align__(256) unsigned char g_static_ws[PKV_STATIC_WS_BYTES];
+}  // namespace pkv
+
+#include <mutex>
+
+// Device address of g_static_ws on the current device, looked up once per
+// device (in host code the array's name is only a host-side stand-in).
+static int static_ws_address(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, pkv::g_static_ws) != cudaSuccess || !p) return PKV_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return PKV_OK;
+}
+
+extern "C" int pkv_decode_attention_static_ws(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
+                                              int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
+                                              int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
+                                              void* out, void* stream) {
+    if (split_tokens <= 0)  // no split: no scratch is used at all
+        return pkv_decode_attention(c, q, block_tables, max_blocks, ctx_lens, slots, B, sm_scale, 0, 0, nullptr,
+                                    nullptr, nullptr, out, stream);
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (B < 0 || max_splits <= 0) return PKV_ERR_INVALID;
+    // layout: [counters B*Hkv int32 | pad to 256 B][m,l: B*Hq*S*2 f32][o: B*Hq*S*d f32]
+    const size_t cnt_bytes = (size_t(B) * size_t(c->num_kv_heads) * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (pkv_splitk_ws_ml_bytes(B, c->num_q_heads, max_splits) + 255) / 256 * 256;
+    const size_t o_bytes = pkv_splitk_ws_o_bytes(B, c->num_q_heads, c->head_dim, max_splits);
+    if (cnt_bytes + ml_bytes + o_bytes > size_t(PKV_STATIC_WS_BYTES)) return PKV_ERR_TOO_LARGE;
+    void* base = nullptr;
+    if ((st = static_ws_address(&base)) != PKV_OK) return st;
+    auto* bytes = static_cast<unsigned char*>(base);
+    auto* counters = reinterpret_cast<int32_t*>(bytes);
+    auto* ws_ml = reinterpret_cast<float*>(bytes + cnt_bytes);
+    auto* ws_o = reinterpret_cast<float*>(bytes + cnt_bytes + ml_bytes);
+    // The array keeps the previous call's contents: the arrival counters must
+    // start at zero, the partials are always written before they are read.
+    if (B > 0 && cudaMemsetAsync(counters, 0, size_t(B) * size_t(c->num_kv_heads) * 4,
+                                 static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return pkv_decode_attention(c, q, block_tables, max_blocks, ctx_lens, slots, B, sm_scale, split_tokens, max_splits,
+                                ws_o, ws_ml, counters, out, stream);
+}

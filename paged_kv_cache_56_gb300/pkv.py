@@ -26,6 +26,8 @@ PKV_ERR_NOT_FOUND = -3
 PKV_ERR_EXISTS = -4
 PKV_ERR_UNSUPPORTED = -5
 PKV_ERR_CUDA = -6
+PKV_ERR_TOO_LARGE = -7
+PKV_STATIC_WS_BYTES = 8 << 20
 
 PKV_DEVERR_BLOCK_ID = 1
 PKV_DEVERR_SLOT = 2
@@ -38,7 +40,8 @@ PKV_DTYPE_INT8 = 1
 
 _NAMES = {PKV_ERR_INVALID: "PKV_ERR_INVALID", PKV_ERR_OOM: "PKV_ERR_OOM",
           PKV_ERR_NOT_FOUND: "PKV_ERR_NOT_FOUND", PKV_ERR_EXISTS: "PKV_ERR_EXISTS",
-          PKV_ERR_UNSUPPORTED: "PKV_ERR_UNSUPPORTED", PKV_ERR_CUDA: "PKV_ERR_CUDA"}
+          PKV_ERR_UNSUPPORTED: "PKV_ERR_UNSUPPORTED", PKV_ERR_CUDA: "PKV_ERR_CUDA",
+          PKV_ERR_TOO_LARGE: "PKV_ERR_TOO_LARGE"}
 
 EXPORTED = (
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_alloc", "pkv_append_block", "pkv_free",
@@ -46,6 +49,7 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_append_kv", "pkv_quantize_full_blocks",
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
+    "pkv_decode_attention_static_ws",
 )
 
 
@@ -99,6 +103,8 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_attention": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP, _I32,
                                                     ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
+            "pkv_decode_attention_static_ws": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP,
+                                                              _I32, ctypes.c_float, _I32, _I32, _VP, _VP]),
             "pkv_splitk_reduce": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP]),
             "pkv_splitk_ws_o_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
             "pkv_splitk_ws_ml_bytes": (ctypes.c_size_t, [_I32, _I32, _I32]),
@@ -311,3 +317,22 @@ def pkv_splitk_reduce(ws_o: torch.Tensor, ws_ml: torch.Tensor, ctx_lens: torch.T
     _check("pkv_splitk_reduce",
            lib().pkv_splitk_reduce(wo, wml, cp, B, num_q_heads, head_dim, split_tokens, max_splits, op,
                                    _stream(stream)))
+
+
+def pkv_decode_attention_static_ws(desc: CacheDesc, q: torch.Tensor, block_tables: torch.Tensor,
+                                   ctx_lens: torch.Tensor, slots, sm_scale: float, out: torch.Tensor,
+                                   split_tokens: int, max_splits: int, stream=None) -> None:
+    """pkv_decode_attention with the split-K scratch in the library's fixed
+    array: allocates nothing (see include/pkv.h for the size limit and the
+    rule that overlapping calls race)."""
+    B = ctx_lens.numel()
+    max_blocks = block_tables.shape[-1] if block_tables.dim() == 2 else 0
+    hq, d = desc.num_q_heads, desc.head_dim
+    qp = _dev(q, "q", torch.bfloat16, B * hq * d)
+    outp = _dev(out, "out", torch.bfloat16, B * hq * d)
+    tp = _dev(block_tables, "block_tables", torch.int32, B * max_blocks)
+    cp = _dev(ctx_lens, "ctx_lens", torch.int32, B)
+    sp = _opt_dev(slots, "slots", torch.int32, B)
+    _check("pkv_decode_attention_static_ws",
+           lib().pkv_decode_attention_static_ws(_desc_ptr(desc), qp, tp, max_blocks, cp, sp, B, float(sm_scale),
+                                                split_tokens, max_splits, outp, _stream(stream)))

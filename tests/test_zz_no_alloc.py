@@ -1,0 +1,65 @@
+"""pkv_decode_attention_static_ws: decode attention for callers that cannot
+allocate device memory while they decode (an engine that gives all free HBM to
+its cache pool at start-up and forbids later allocations, code running inside
+such an engine, a latency-critical loop that must not pay for cudaMalloc's
+implicit synchronisation). Its split-K scratch is a fixed array inside the
+library. Two calls in a row, through the C ABI, must agree with the regular
+entry point, which uses a workspace the caller allocated."""
+
+import pytest
+import torch
+
+from harness import Workload, assert_close
+from libpkv import ensure_built
+from paged_kv_cache_56_gb300 import pkv, synth
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny_int8": dict(num_layers=1, prior=(1, 17, 33, 100), Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=True,
+                      split_tokens=32, max_blocks=9),
+    "tiny_bf16": dict(num_layers=1, prior=(15, 16, 31, 0), Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=False,
+                      split_tokens=16, max_blocks=9),
+    "gqa_int8_2000": dict(num_layers=1, prior=(2000, 1999, 1500, 2047), Hq=16, Hkv=8, d=128, bs=16,
+                          num_blocks=600, int8=True, split_tokens=128, max_blocks=130, head_scale=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_static_ws_matches_regular_entry_point(name):
+    ensure_built()
+    w = Workload(seed=4321, **CASES[name])
+    c, bufs, lc = w.cache, w.bufs, w.cache.layers[0]
+    plan = c.plan_step(w.req_ids)
+    bufs.upload(plan)
+    B = w.B
+    pos = torch.tensor(plan.positions, dtype=torch.int64)
+    q = w.q(0, 0, w.req_ids)
+    pkv.pkv_append_kv(lc.desc, w.kv(0, synth.KIND_K, w.req_ids, pos), w.kv(0, synth.KIND_V, w.req_ids, pos),
+                      bufs.blk[:B], bufs.off[:B], bufs.slot[:B])
+    if c.int8:
+        pkv.pkv_quantize_full_blocks(lc.desc, bufs.fill[:B], bufs.slot[:B])
+    ref = torch.empty((B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_decode_attention(lc.desc, q, bufs.tab[:B], bufs.ctx[:B], bufs.slot[:B], w.sm_scale, ref,
+                             bufs.split_tokens, bufs.max_splits, bufs.ws_o, bufs.ws_ml, bufs.ws_count)
+    ref = ref.float().cpu().numpy()
+    for call in range(2):
+        out = torch.full((B, w.Hq, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pkv.pkv_decode_attention_static_ws(lc.desc, q, bufs.tab[:B], bufs.ctx[:B], bufs.slot[:B], w.sm_scale, out,
+                                           bufs.split_tokens, bufs.max_splits)
+        assert_close(out.float().cpu().numpy(), ref, f"{name} call {call + 1}")
+    assert w.error_bits() == 0
+
+
+def test_static_ws_rejects_requests_beyond_its_size():
+    ensure_built()
+    w = Workload(seed=1, **CASES["tiny_int8"])
+    lc, bufs = w.cache.layers[0], w.bufs
+    B, max_blocks = w.B, 4096
+    tab = torch.full((B, max_blocks), -1, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    q = w.q(0, 0, w.req_ids)
+    # 4096 splits x 4 sequences x 4 heads x (64 + 2) floats is more than the fixed array holds
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_attention_static_ws(lc.desc, q, tab, bufs.ctx[:B], bufs.slot[:B], w.sm_scale, out, 16, 4096)
+    assert e.value.code == pkv.PKV_ERR_TOO_LARGE
