@@ -229,6 +229,8 @@ def run_device(args, wl, rank, world):
     L, R, B = wl["L"], wl["repeat"], wl["B"]
     Hq, Hkv, d, bs = wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
     graph = not args.eager
+    from paged_kv_cache_56_gb300 import pkv
+    pkv.pkv_set_programmatic_launch(not args.no_pdl)
     # inputs for every step, resident in HBM before timing
     inputs = [bench.step_inputs(s) for s in range(args.warmup + args.steps)]
     gs = None
@@ -390,6 +392,7 @@ def main():
     ap.add_argument("--eager", action="store_true", help="launch each kernel from Python instead of a CUDA graph")
     ap.add_argument("--split", type=int, default=None, help="split_tokens (default: sized to one wave)")
     ap.add_argument("--separate-merge", action="store_true", help="merge split-K partials in a second kernel")
+    ap.add_argument("--no-pdl", action="store_true", help="launch kernels without programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -437,7 +440,8 @@ def main():
                    "ctx_range": list(r["ctx"]), "l2": "inputs larger than L2 (per-step KV >> 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "CUDA graph per step" if r["graph"] else "eager",
-                   "split_merge": "separate kernel" if args.separate_merge else "fused (last split merges)"},
+                   "split_merge": "separate kernel" if args.separate_merge else "fused (last split merges)",
+                   "programmatic_dependent_launch": not args.no_pdl},
         "tokens_per_s": round(wl["B"] * world / (ms_step * 1e-3), 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

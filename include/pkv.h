@@ -230,6 +230,19 @@ int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_
 size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits);
 size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
 
+/* Process-wide switch (default off) for programmatic dependent launch: with
+ * it on, every kernel of this library is launched so that it may start while
+ * the previous kernel on the stream is still running, and each waits for that
+ * kernel to complete before it reads anything the kernel could have written.
+ * The one exception is the early start of pkv_decode_attention: before its
+ * wait it already reads ctx_lens, block_tables, slots, and the cache blocks
+ * (and scales) below the block holding each sequence's last token. With the
+ * switch on, those must therefore not be written by the kernel launched just
+ * before on the same stream (this library's append and quantize kernels
+ * write only the last block). Lets a decode step's per-layer kernels overlap
+ * each other's launch and drain. */
+int pkv_set_programmatic_launch(int enable);
+
 /* Bytes of the library-owned split-K scratch array used by
  * pkv_decode_attention_static_ws (8 MiB, held on every GPU that loads the
  * library for the life of the process). */

@@ -388,7 +388,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
+    pdl_launch_dependents();
 
+    // Before pdl_wait() this kernel reads only what no preceding kernel of the
+    // step writes: context lengths, block tables, slots, and the blocks (and
+    // scales) below the one holding token ctx-1 -- the only block this step's
+    // append / quantize-on-fill may have written.
     int ctx = p.ctx_lens[b];
     if (ctx < 0 || ctx > p.max_blocks * p.bs) {
         if (tid == 0 && j == 0) report(p.err, kErrCtxLen);
@@ -404,6 +409,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     const int nt = (npool + kTile - 1) / kTile;
     const int blk0 = t0 / p.bs;
     const int nblk = npool > 0 ? min((pool_end - 1) / p.bs - blk0 + 1, p.tab_cap) : 0;
+    const int last_blk = ctx > 0 ? (ctx - 1) / p.bs : 0;                       // may change this step
+    const int nt_stable = max(0, min(nt, (last_blk * p.bs - t0) / kTile));      // tiles below it
+    const int nblk_stable = max(0, min(nblk, last_blk - blk0));
 
     const uint32_t bar0 = smem_addr(bars);
     const uint32_t stage0 = smem_addr(stages);
@@ -440,20 +448,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
         bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
     };
-    if (lane == 0)
-        for (int s = 0; s < STAGES; ++s) {
-            const int tile = warp + s * kWarps;
-            if (tile < nt) issue(tile, s);
-        }
-
-    if (INT8) {
-        for (int i = tid; i < nblk; i += kThreads) {
+    auto load_scales = [&](int lo, int hi) {
+        for (int i = lo + tid; i < hi; i += kThreads) {
             const int id = tab[i];
             float2 sc = make_float2(0.f, 0.f);
             if (id >= 0) sc = *reinterpret_cast<const float2*>(p.scales + (size_t(id) * p.Hkv + kvh) * 2);
             bsc[i] = sc;
         }
-    }
+    };
+    if (lane == 0)
+        for (int s = 0; s < STAGES; ++s) {
+            const int tile = warp + s * kWarps;
+            if (tile < nt_stable) issue(tile, s);
+        }
+    if (INT8) load_scales(0, nblk_stable);
+
+    pdl_wait();  // the previous kernel (and so the previous layer) has completed
+
+    if (lane == 0)
+        for (int s = 0; s < STAGES; ++s) {
+            const int tile = warp + s * kWarps;
+            if (tile >= nt_stable && tile < nt) issue(tile, s);
+        }
+    if (INT8) load_scales(nblk_stable, nblk);
 
     const uint16_t* qbase = p.q + (size_t(b) * p.Hq + size_t(kvh) * G) * D;
     uint32_t qf[D / 16][2];
@@ -651,6 +668,8 @@ __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restr
     extern __shared__ float cw[];  // [max_splits] weights
     __shared__ float red[32];
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
     int ctx = ctx_lens[b];
     if (ctx < 0) ctx = 0;
     int ns = (ctx + split_tokens - 1) / split_tokens;

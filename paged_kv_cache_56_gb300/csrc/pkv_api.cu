@@ -5,7 +5,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/pkv.h"
 #include "kernels.cuh"
@@ -25,6 +27,8 @@ __global__ void __launch_bounds__(256) append_kernel(const uint16_t* __restrict_
                                                      int32_t max_slots, int int8_mode, void* k_dst,
                                                      void* v_dst, int32_t* err) {
     constexpr int CH = D / 8;  // 16-byte chunks per row
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t rows = int64_t(T) * 2 * Hkv;
     if (e >= rows * CH) return;
@@ -74,6 +78,8 @@ __global__ void __launch_bounds__(128) quantize_kernel(const uint16_t* __restric
                                                        int32_t max_slots, int8_t* k_pool, int8_t* v_pool,
                                                        float* scales, int32_t* err) {
     constexpr int CH = D / 8;
+    pdl_launch_dependents();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t slab = int64_t(blockIdx.x) * 4 + warp;
     if (slab >= int64_t(M) * 2 * Hkv) return;
@@ -161,6 +167,27 @@ static int check_desc(const pkv_cache_desc* c) {
 
 static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
+static std::atomic<int> g_pdl{0};
+
+// Launches with the programmatic-stream-serialization attribute when enabled
+// (pkv_set_programmatic_launch), plainly otherwise.
+template <typename... Params, typename... Args>
+static int launch(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (g_pdl.load(std::memory_order_relaxed)) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+}
+
 using DecodeFn = void (*)(DecodeParams);
 
 template <int D, bool INT8, bool SPLIT>
@@ -217,6 +244,11 @@ using namespace pkv;
 
 extern "C" {
 
+int pkv_set_programmatic_launch(int enable) {
+    g_pdl.store(enable ? 1 : 0);
+    return PKV_OK;
+}
+
 size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits) {
     if (B < 0 || Hq < 0 || head_dim < 0 || max_splits < 0) return 0;
     return size_t(B) * size_t(Hq) * size_t(max_splits) * size_t(head_dim) * sizeof(float);
@@ -244,15 +276,12 @@ int pkv_append_kv(const pkv_cache_desc* c, const void* k, const void* v, const i
     auto s = static_cast<cudaStream_t>(stream);
     const auto* kk = static_cast<const uint16_t*>(k);
     const auto* vv = static_cast<const uint16_t*>(v);
+    const int i8 = int8 ? 1 : 0;
     if (c->head_dim == 128)
-        append_kernel<128><<<unsigned(grid), 256, 0, s>>>(kk, vv, block_ids, offsets, slots, T, c->num_kv_heads,
-                                                          c->block_size, c->num_blocks, c->max_slots, int8, kd,
-                                                          vd, c->err_word);
-    else
-        append_kernel<64><<<unsigned(grid), 256, 0, s>>>(kk, vv, block_ids, offsets, slots, T, c->num_kv_heads,
-                                                         c->block_size, c->num_blocks, c->max_slots, int8, kd,
-                                                         vd, c->err_word);
-    return cuda_status(cudaGetLastError());
+        return launch(append_kernel<128>, dim3(unsigned(grid)), dim3(256), 0, s, kk, vv, block_ids, offsets, slots, T,
+                      c->num_kv_heads, c->block_size, c->num_blocks, c->max_slots, i8, kd, vd, c->err_word);
+    return launch(append_kernel<64>, dim3(unsigned(grid)), dim3(256), 0, s, kk, vv, block_ids, offsets, slots, T,
+                  c->num_kv_heads, c->block_size, c->num_blocks, c->max_slots, i8, kd, vd, c->err_word);
 }
 
 static int quantize_common(const pkv_cache_desc* c, const void* k_src, const void* v_src, int from_tail,
@@ -272,14 +301,11 @@ static int quantize_common(const pkv_cache_desc* c, const void* k_src, const voi
     auto* kp = static_cast<int8_t*>(c->k_pool);
     auto* vp = static_cast<int8_t*>(c->v_pool);
     if (c->head_dim == 128)
-        quantize_kernel<128><<<unsigned(grid), 128, 0, s>>>(ks, vs, from_tail, block_ids, slots, M, c->num_kv_heads,
-                                                            c->block_size, c->num_blocks, c->max_slots, kp, vp,
-                                                            c->scales, c->err_word);
-    else
-        quantize_kernel<64><<<unsigned(grid), 128, 0, s>>>(ks, vs, from_tail, block_ids, slots, M, c->num_kv_heads,
-                                                           c->block_size, c->num_blocks, c->max_slots, kp, vp,
-                                                           c->scales, c->err_word);
-    return cuda_status(cudaGetLastError());
+        return launch(quantize_kernel<128>, dim3(unsigned(grid)), dim3(128), 0, s, ks, vs, from_tail, block_ids, slots,
+                      M, c->num_kv_heads, c->block_size, c->num_blocks, c->max_slots, kp, vp, c->scales,
+                      c->err_word);
+    return launch(quantize_kernel<64>, dim3(unsigned(grid)), dim3(128), 0, s, ks, vs, from_tail, block_ids, slots, M,
+                  c->num_kv_heads, c->block_size, c->num_blocks, c->max_slots, kp, vp, c->scales, c->err_word);
 }
 
 int pkv_quantize_full_blocks(const pkv_cache_desc* c, const int32_t* block_ids, const int32_t* slots,
@@ -306,12 +332,10 @@ static int launch_reduce(const float* ws_o, const float* ws_ml, const int32_t* c
     const dim3 grid{unsigned(Hq), unsigned(B), 1u};
     auto* o = static_cast<uint16_t*>(out);
     if (head_dim == 128)
-        splitk_reduce_kernel<128><<<grid, 128, smem, s>>>(ws_o, ws_ml, ctx_lens, Hq, split_tokens, max_splits, o,
-                                                          err);
-    else
-        splitk_reduce_kernel<64><<<grid, 128, smem, s>>>(ws_o, ws_ml, ctx_lens, Hq, split_tokens, max_splits, o,
-                                                         err);
-    return cuda_status(cudaGetLastError());
+        return launch(splitk_reduce_kernel<128>, grid, dim3(128), smem, s, ws_o, ws_ml, ctx_lens, Hq, split_tokens,
+                      max_splits, o, err);
+    return launch(splitk_reduce_kernel<64>, grid, dim3(128), smem, s, ws_o, ws_ml, ctx_lens, Hq, split_tokens,
+                  max_splits, o, err);
 }
 
 int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_lens, int32_t B, int32_t Hq,
@@ -401,8 +425,7 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     DecodeFn fn = pick_decode(c->head_dim, g, int8, split, &index);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
-    fn<<<grid, kThreads, smem, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if ((st = launch(fn, grid, dim3(kThreads), smem, s, p)) != PKV_OK) return st;
     if (!split || fuse) return PKV_OK;
     return launch_reduce(ws_o, ws_ml, ctx_lens, B, c->num_q_heads, c->head_dim, split_tokens, max_splits, out,
                          c->err_word, stream);

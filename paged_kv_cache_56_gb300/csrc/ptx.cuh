@@ -121,6 +121,14 @@ __device__ __forceinline__ void s8x4_to_f4(uint32_t w, float2& lo, float2& hi) {
     hi = __fadd2_rn(b, bias);
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now / wait until the previous kernel has completed and its
+// memory is visible. Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -49,7 +49,7 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_append_kv", "pkv_quantize_full_blocks",
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
-    "pkv_decode_attention_static_ws",
+    "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch",
 )
 
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_attention": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP, _I32,
                                                     ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
+            "pkv_set_programmatic_launch": (ctypes.c_int, [ctypes.c_int]),
             "pkv_decode_attention_static_ws": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP,
                                                               _I32, ctypes.c_float, _I32, _I32, _VP, _VP]),
             "pkv_splitk_reduce": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP]),
@@ -267,6 +268,10 @@ def pkv_quantize_blocks_from(desc: CacheDesc, k_src: torch.Tensor, v_src: torch.
     bp = _dev(block_ids, "block_ids", torch.int32, M)
     _check("pkv_quantize_blocks_from",
            lib().pkv_quantize_blocks_from(_desc_ptr(desc), kp, vp, bp, M, _stream(stream)))
+
+
+def pkv_set_programmatic_launch(enable: bool) -> None:
+    _check("pkv_set_programmatic_launch", lib().pkv_set_programmatic_launch(1 if enable else 0))
 
 
 def pkv_splitk_ws_o_bytes(B: int, Hq: int, head_dim: int, max_splits: int) -> int:

@@ -15,7 +15,7 @@ import torch
 
 from oracle.attention import decode_attention
 from oracle.cache import SequenceHistory
-from paged_kv_cache_56_gb300 import synth
+from paged_kv_cache_56_gb300 import pkv, synth
 from paged_kv_cache_56_gb300.runtime import (GraphStep, PagedKVCache, StepBuffers, decode_step,
                                               plan_split_tokens, prefill)
 
@@ -60,6 +60,8 @@ class Workload:
         self.graph = graph
         self.R = repeat
         self.gs = None
+        # the benchmark's launch configuration uses programmatic dependent launch
+        pkv.pkv_set_programmatic_launch(graph)
         for r, n in zip(self.req_ids, self.prior):
             self.cache.add_sequence(r, -(-n // bs))
         for li in range(num_layers):
