@@ -209,6 +209,23 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
                          int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
                          float* ws_o, float* ws_ml, int32_t* ws_count, void* out, void* stream);
 
+/* One layer's whole decode step in one kernel: for each sequence b, append
+ * the new rows k_new[b], v_new[b] ([B][Hkv][d] bf16, device) as token
+ * ctx_lens[b] - 1 (BF16: into block block_tables[b][(ctx_lens[b]-1)/bs],
+ * which must already be allocated; INT8: into the tail of slots[b]); in INT8
+ * mode, if that token fills its block, quantize the block into the pool
+ * exactly as pkv_quantize_full_blocks does; then attend over ctx_lens[b]
+ * tokens exactly as pkv_decode_attention does. The result equals
+ * pkv_append_kv + pkv_quantize_full_blocks + pkv_decode_attention; the
+ * row is written (and the block quantized) by the CTA that reads it, so no
+ * separate kernel sits between the layer's inputs and its attention. All
+ * other arguments are those of pkv_decode_attention. */
+int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
+                    const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                    const int32_t* slots, int32_t B, float sm_scale, int32_t split_tokens,
+                    int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count, void* out,
+                    void* stream);
+
 /* CTAs of the decode kernel for this cache shape that fit on one SM at once
  * (registers and shared memory), for a given split_tokens (0 = none) and
  * max_blocks; a caller sizes its splits so that B * Hkv * splits fills

@@ -24,7 +24,7 @@
 #include "ptx.cuh"
 
 #ifndef PKV_STAGES_INT8
-#define PKV_STAGES_INT8 3  // bulk-copy stages per warp, INT8 cache (4 KB each at d = 128)
+#define PKV_STAGES_INT8 2  // bulk-copy stages per warp, INT8 cache (4 KB each at d = 128)
 #endif
 #ifndef PKV_STAGES_BF16
 #define PKV_STAGES_BF16 2  // bulk-copy stages per warp, bf16 cache (8 KB each at d = 128)
@@ -54,6 +54,8 @@ struct DecodeParams {
     const void* k_tail;
     const void* v_tail;
     const uint16_t* q;
+    const uint16_t* k_new;  // [B][Hkv][D] rows appended this step (nullable: cache already written)
+    const uint16_t* v_new;
     const int32_t* block_tables;
     const int32_t* ctx_lens;
     const int32_t* slots;
@@ -178,12 +180,12 @@ struct SmemRows {
         return v;
     }
 };
-struct GmemRows {
+struct GmemRows {  // rows this kernel may itself have written: read through L2
     const uint8_t* base;
     int row;
-    __device__ __forceinline__ uint4 ld16(int r, int off) const { return ldg128(base + size_t(r) * row + off); }
+    __device__ __forceinline__ uint4 ld16(int r, int off) const { return ldcg128(base + size_t(r) * row + off); }
     __device__ __forceinline__ uint2 ld8(int r, int off) const {
-        return *reinterpret_cast<const uint2*>(base + size_t(r) * row + off);
+        return __ldcg(reinterpret_cast<const uint2*>(base + size_t(r) * row + off));
     }
 };
 
@@ -356,6 +358,54 @@ __device__ __forceinline__ int load_q_frags(const uint16_t* qrow, int g, int t, 
     return e;
 }
 
+// Quantizes one (block, kv head, K|V) slab of bs x D bf16 values with one
+// warp, the definition of the INT8 cache ("轻量级推理引擎实战" §3 under this
+// build's readings): scale = max|x| / 127 by IEEE fp32 division, or 1.0 when
+// max|x| < 1e-6; code = clamp(round-half-even(x / scale), -127, 127) with
+// IEEE fp32 division. Source rows are `row_stride` elements apart; the codes
+// are written to `dst` as bs x D bytes and the scale to *scale_out.
+// COHERENT: read the source through L2 (it was written earlier in this kernel).
+template <int D, bool COHERENT>
+__device__ __forceinline__ void quantize_slab(int lane, const uint16_t* base, int64_t row_stride, int bs,
+                                              int8_t* dst, float* scale_out) {
+    constexpr int CH = D / 8;
+    const int nch = bs * CH;
+    auto load = [&](int c) {
+        const uint16_t* ptr = base + int64_t(c / CH) * row_stride + (c % CH) * 8;
+        return COHERENT ? ldcg128(ptr) : ldg128(ptr);
+    };
+    float mx = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+        const uint4 w = load(c);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f2(ws[i]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float scale = mx < 1e-6f ? 1.0f : __fdiv_rn(mx, 127.0f);
+    for (int c = lane; c < nch; c += 32) {
+        const uint4 w = load(c);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f2(ws[i]);
+            int q0 = __float2int_rn(__fdiv_rn(f.x, scale));
+            int q1 = __float2int_rn(__fdiv_rn(f.y, scale));
+            q0 = min(127, max(-127, q0));
+            q1 = min(127, max(-127, q1));
+            const uint32_t pair = (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8);
+            packed[i >> 1] |= pair << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint2*>(dst + int64_t(c) * 8) = make_uint2(packed[0], packed[1]);
+    }
+    if (lane == 0) *scale_out = scale;
+}
+
 // Waits for an mbarrier phase for at most ~1 s of GPU time. A waiting warp
 // sleeps in try_wait (up to 2 us per poll) rather than spinning, so it does
 // not take issue slots from warps that have data.
@@ -452,7 +502,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         for (int i = lo + tid; i < hi; i += kThreads) {
             const int id = tab[i];
             float2 sc = make_float2(0.f, 0.f);
-            if (id >= 0) sc = *reinterpret_cast<const float2*>(p.scales + (size_t(id) * p.Hkv + kvh) * 2);
+            if (id >= 0) sc = __ldcg(reinterpret_cast<const float2*>(p.scales + (size_t(id) * p.Hkv + kvh) * 2));
             bsc[i] = sc;
         }
     };
@@ -464,6 +514,49 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     if (INT8) load_scales(0, nblk_stable);
 
     pdl_wait();  // the previous kernel (and so the previous layer) has completed
+
+    // ---- fused step update: the split holding token ctx-1 writes that token's
+    // K/V row (given in k_new / v_new) and, in INT8 mode, quantizes its block if
+    // the row filled it -- before any read of that block.
+    if (p.k_new != nullptr && ctx > 0 && t0 <= ctx - 1 && ctx - 1 < t1) {
+        const int pos = ctx - 1, off = pos % p.bs;
+        const int bl = pos / p.bs - blk0;
+        const int id = (bl >= 0 && bl < nblk) ? tab[bl] : -1;
+        const int slot = (INT8 && p.slots) ? p.slots[b] : -1;
+        const bool ok = INT8 ? (slot >= 0 && slot < p.max_slots) : (id >= 0);
+        if (ok) {
+            const size_t row = INT8 ? (size_t(slot) * p.Hkv + kvh) * p.bs + off
+                                    : (size_t(id) * p.Hkv + kvh) * p.bs + off;
+            uint16_t* dk = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.k_tail : p.k_pool)) + row * D;
+            uint16_t* dv = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.v_tail : p.v_pool)) + row * D;
+            const uint16_t* sk = p.k_new + (size_t(b) * p.Hkv + kvh) * D;
+            const uint16_t* sv = p.v_new + (size_t(b) * p.Hkv + kvh) * D;
+            for (int c = tid; c < 2 * (D / 8); c += kThreads) {
+                const int kv = c / (D / 8), ch = c % (D / 8);
+                *reinterpret_cast<uint4*>((kv ? dv : dk) + ch * 8) = ldg128((kv ? sv : sk) + ch * 8);
+            }
+            if (!INT8) fence_proxy_async_global();  // the pool row is read by a bulk copy below
+        } else if (tid == 0) {
+            report(p.err, INT8 ? kErrSlot : kErrBlockId);
+        }
+        __syncthreads();
+        if (INT8 && ok && (pos + 1) % p.bs == 0) {
+            if (id >= 0) {
+                if (warp < 2) {
+                    const uint16_t* src = static_cast<const uint16_t*>(warp ? p.v_tail : p.k_tail) +
+                                          (size_t(slot) * p.Hkv + kvh) * p.bs * D;
+                    int8_t* dst = static_cast<int8_t*>(const_cast<void*>(warp ? p.v_pool : p.k_pool)) +
+                                  (size_t(id) * p.Hkv + kvh) * p.bs * D;
+                    quantize_slab<D, true>(lane, src, D, p.bs, dst,
+                                           const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + warp);
+                    fence_proxy_async_global();  // the codes are read by a bulk copy below
+                }
+            } else if (tid == 0) {
+                report(p.err, kErrBlockId);
+            }
+            __syncthreads();
+        }
+    }
 
     if (lane == 0)
         for (int s = 0; s < STAGES; ++s) {

@@ -77,7 +77,6 @@ __global__ void __launch_bounds__(128) quantize_kernel(const uint16_t* __restric
                                                        int32_t Hkv, int32_t bs, int32_t num_blocks,
                                                        int32_t max_slots, int8_t* k_pool, int8_t* v_pool,
                                                        float* scales, int32_t* err) {
-    constexpr int CH = D / 8;
     pdl_launch_dependents();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -106,38 +105,8 @@ __global__ void __launch_bounds__(128) quantize_kernel(const uint16_t* __restric
         base = (kv ? v_src : k_src) + (int64_t(m) * bs * Hkv + h) * D;
         row_stride = int64_t(Hkv) * D;
     }
-    const int nch = bs * CH;
-    float mx = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-        const uint4 w = ldg128(base + int64_t(c / CH) * row_stride + (c % CH) * 8);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = bf16x2_to_f2(ws[i]);
-            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    const float scale = mx < 1e-6f ? 1.0f : __fdiv_rn(mx, 127.0f);
     int8_t* dst = (kv ? v_pool : k_pool) + (int64_t(blk) * Hkv + h) * bs * D;
-    for (int c = lane; c < nch; c += 32) {
-        const uint4 w = ldg128(base + int64_t(c / CH) * row_stride + (c % CH) * 8);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = bf16x2_to_f2(ws[i]);
-            int q0 = __float2int_rn(__fdiv_rn(f.x, scale));
-            int q1 = __float2int_rn(__fdiv_rn(f.y, scale));
-            q0 = min(127, max(-127, q0));
-            q1 = min(127, max(-127, q1));
-            const uint32_t pair = (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8);
-            packed[i >> 1] |= pair << (16 * (i & 1));
-        }
-        *reinterpret_cast<uint2*>(dst + int64_t(c) * 8) = make_uint2(packed[0], packed[1]);
-    }
-    if (lane == 0) scales[(int64_t(blk) * Hkv + h) * 2 + kv] = scale;
+    quantize_slab<D, false>(lane, base, row_stride, bs, dst, scales + (int64_t(blk) * Hkv + h) * 2 + kv);
 }
 
 // ---------------------------------------------------------------------------
@@ -366,10 +335,10 @@ int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_
     return n;
 }
 
-int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables, int32_t max_blocks,
-                         const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
-                         int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count,
-                         void* out, void* stream) {
+static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
+                       const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
+                       int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml,
+                       int32_t* ws_count, void* out, void* stream) {
     int st = check_desc(c);
     if (st != PKV_OK) return st;
     if (B < 0 || max_blocks <= 0 || split_tokens < 0 || !(sm_scale == sm_scale)) return PKV_ERR_INVALID;
@@ -399,6 +368,8 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     p.k_tail = c->k_tail;
     p.v_tail = c->v_tail;
     p.q = static_cast<const uint16_t*>(q);
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
     p.block_tables = block_tables;
     p.ctx_lens = ctx_lens;
     p.slots = slots;
@@ -429,6 +400,23 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
     if (!split || fuse) return PKV_OK;
     return launch_reduce(ws_o, ws_ml, ctx_lens, B, c->num_q_heads, c->head_dim, split_tokens, max_splits, out,
                          c->err_word, stream);
+}
+
+int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
+                         int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count,
+                         void* out, void* stream) {
+    return decode_impl(c, q, nullptr, nullptr, block_tables, max_blocks, ctx_lens, slots, B, sm_scale, split_tokens,
+                       max_splits, ws_o, ws_ml, ws_count, out, stream);
+}
+
+int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
+                    const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
+                    int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml,
+                    int32_t* ws_count, void* out, void* stream) {
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID;
+    return decode_impl(c, q, k_new, v_new, block_tables, max_blocks, ctx_lens, slots, B, sm_scale, split_tokens,
+                       max_splits, ws_o, ws_ml, ws_count, out, stream);
 }
 
 }  // extern "C"

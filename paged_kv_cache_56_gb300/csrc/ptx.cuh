@@ -93,6 +93,23 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+// Global load through L2 only: sees global writes made earlier in this kernel
+// by other threads of the CTA (after a barrier), unlike the read-only path.
+__device__ __forceinline__ uint4 ldcg128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// Orders this thread's earlier generic-proxy global writes before later
+// asynchronous-proxy (bulk copy) reads of the same addresses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ldg128(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -49,7 +49,7 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_append_kv", "pkv_quantize_full_blocks",
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
-    "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch",
+    "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step",
 )
 
 
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
             "pkv_set_programmatic_launch": (ctypes.c_int, [ctypes.c_int]),
+            "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _I32,
+                                               ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_attention_static_ws": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP,
                                                               _I32, ctypes.c_float, _I32, _I32, _VP, _VP]),
             "pkv_splitk_reduce": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP]),
@@ -309,6 +311,30 @@ def pkv_decode_attention(desc: CacheDesc, q: torch.Tensor, block_tables: torch.T
     _check("pkv_decode_attention",
            lib().pkv_decode_attention(_desc_ptr(desc), qp, tp, max_blocks, cp, sp, B, float(sm_scale),
                                       split_tokens, max_splits, wo, wml, wc, outp, _stream(stream)))
+
+
+def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    block_tables: torch.Tensor, ctx_lens: torch.Tensor, slots, sm_scale: float, out: torch.Tensor,
+                    split_tokens: int = 0, max_splits: int = 0, ws_o=None, ws_ml=None, ws_count=None,
+                    stream=None) -> None:
+    B = ctx_lens.numel()
+    max_blocks = block_tables.shape[-1] if block_tables.dim() == 2 else 0
+    hq, hkv, d = desc.num_q_heads, desc.num_kv_heads, desc.head_dim
+    qp = _dev(q, "q", torch.bfloat16, B * hq * d)
+    kp = _dev(k_new, "k_new", torch.bfloat16, B * hkv * d)
+    vp = _dev(v_new, "v_new", torch.bfloat16, B * hkv * d)
+    outp = _dev(out, "out", torch.bfloat16, B * hq * d)
+    tp = _dev(block_tables, "block_tables", torch.int32, B * max_blocks)
+    cp = _dev(ctx_lens, "ctx_lens", torch.int32, B)
+    sp = _opt_dev(slots, "slots", torch.int32, B)
+    wo = wml = wc = None
+    if split_tokens > 0:
+        wo = _dev(ws_o, "ws_o", torch.float32, B * hq * max_splits * d)
+        wml = _dev(ws_ml, "ws_ml", torch.float32, B * hq * max_splits * 2)
+        wc = _opt_dev(ws_count, "ws_count", torch.int32, B * hkv)
+    _check("pkv_decode_step",
+           lib().pkv_decode_step(_desc_ptr(desc), qp, kp, vp, tp, max_blocks, cp, sp, B, float(sm_scale),
+                                 split_tokens, max_splits, wo, wml, wc, outp, _stream(stream)))
 
 
 def pkv_splitk_reduce(ws_o: torch.Tensor, ws_ml: torch.Tensor, ctx_lens: torch.Tensor, num_q_heads: int,

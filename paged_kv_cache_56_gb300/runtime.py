@@ -347,8 +347,10 @@ class GraphStep:
     capture time.
     """
 
-    def __init__(self, cache: PagedKVCache, bufs: StepBuffers, sm_scale: float, repeat: int = 1):
+    def __init__(self, cache: PagedKVCache, bufs: StepBuffers, sm_scale: float, repeat: int = 1,
+                 fused: bool = True):
         self.cache, self.bufs, self.sm_scale, self.R = cache, bufs, sm_scale, repeat
+        self.fused = fused  # one pkv_decode_step per layer instead of append + quantize + attention
         B, dev = bufs.B, cache.device
         if B == 0:
             raise ValueError("upload a plan before capturing")
@@ -362,20 +364,28 @@ class GraphStep:
 
     def launches_per_step(self) -> int:
         per_attn = 2 if (self.bufs.split_tokens and self.bufs.ws_count is None) else 1
-        return self.cache.L * (1 + (1 if self.cache.int8 else 0) + self.R * per_attn)
+        update = 0 if self.fused else 1 + (1 if self.cache.int8 else 0)
+        return self.cache.L * (update + self.R * per_attn)
 
     def _layers(self, attention_only: bool = False) -> None:
         c, b = self.cache, self.bufs
         B = b.B
         for li, lc in enumerate(c.layers):
-            if not attention_only:
+            fused_here = self.fused and not attention_only
+            if not attention_only and not self.fused:
                 pkv.pkv_append_kv(lc.desc, self.k[li], self.v[li], b.blk[:B], b.off[:B], b.slot[:B])
                 if c.int8:
                     pkv.pkv_quantize_full_blocks(lc.desc, b.fill[:B], b.slot[:B])
             for r in range(self.R):
                 qi = li * self.R + r
-                pkv.pkv_decode_attention(lc.desc, self.q[qi], b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
-                                         self.out[qi], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
+                if fused_here and r == 0:
+                    pkv.pkv_decode_step(lc.desc, self.q[qi], self.k[li], self.v[li], b.tab[:B], b.ctx[:B],
+                                        b.slot[:B], self.sm_scale, self.out[qi], b.split_tokens, b.max_splits,
+                                        b.ws_o, b.ws_ml, b.ws_count)
+                else:
+                    pkv.pkv_decode_attention(lc.desc, self.q[qi], b.tab[:B], b.ctx[:B], b.slot[:B],
+                                             self.sm_scale, self.out[qi], b.split_tokens, b.max_splits, b.ws_o,
+                                             b.ws_ml, b.ws_count)
 
     def run_eager(self) -> None:
         self._layers()

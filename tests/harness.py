@@ -39,7 +39,8 @@ class Workload:
     def __init__(self, seed: int, num_layers: int, prior, Hq: int, Hkv: int, d: int, bs: int,
                  num_blocks: int, int8: bool, split_tokens: int = 0, max_blocks: int | None = None,
                  head_scale: bool = False, outliers: bool = False, shuffle: bool = True,
-                 req_ids=None, device="cuda", fused_merge: bool = True, graph: bool = False, repeat: int = 1):
+                 req_ids=None, device="cuda", fused_merge: bool = True, graph: bool = False, repeat: int = 1,
+                 fused_step: bool | None = None):
         self.seed, self.L, self.prior = seed, num_layers, list(prior)
         self.Hq, self.Hkv, self.d, self.bs = Hq, Hkv, d, bs
         self.int8 = int8
@@ -60,6 +61,9 @@ class Workload:
         self.graph = graph
         self.R = repeat
         self.gs = None
+        # fused_step: one pkv_decode_step per layer (the benchmark's path);
+        # default on for graph replay, off for the eager three-kernel path
+        self.fused_step = graph if fused_step is None else fused_step
         # the benchmark's launch configuration uses programmatic dependent launch
         pkv.pkv_set_programmatic_launch(graph)
         for r, n in zip(self.req_ids, self.prior):
@@ -111,7 +115,7 @@ class Workload:
         q = torch.stack([self.q_for(qi, t, self.req_ids) for qi in range(self.L * self.R)])
         kn = torch.stack([self.kv(li, synth.KIND_K, self.req_ids, pos) for li in range(self.L)])
         vn = torch.stack([self.kv(li, synth.KIND_V, self.req_ids, pos) for li in range(self.L)])
-        if not self.graph and self.R == 1:
+        if not self.graph and self.R == 1 and not self.fused_step:
             out = torch.empty((self.L, self.B, self.Hq, self.d), dtype=torch.bfloat16, device=self.device)
             decode_step(self.cache, self.bufs, self.req_ids, list(q), list(kn), list(vn), list(out), self.sm_scale)
             self.step_no += 1
@@ -120,7 +124,7 @@ class Workload:
         self.bufs.upload(plan)
         first = self.gs is None
         if first:
-            self.gs = GraphStep(self.cache, self.bufs, self.sm_scale, self.R)
+            self.gs = GraphStep(self.cache, self.bufs, self.sm_scale, self.R, fused=self.fused_step)
         self.gs.q.copy_(q)
         self.gs.k.copy_(kn)
         self.gs.v.copy_(vn)

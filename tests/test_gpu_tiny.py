@@ -78,3 +78,31 @@ def test_graph_replay_matches_oracle(int8):
             for rep in range(2):
                 assert_close(out[rep, i], w.oracle_out(0, i, t, rep), f"step {t} seq {i} rep {rep}")
     assert w.error_bits() == 0
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+@pytest.mark.parametrize("split", [0, 32])
+def test_fused_step_equals_separate_kernels(int8, split):
+    """pkv_decode_step (append + quantize-on-fill + attention in one kernel)
+    gives the same bytes as the three separate kernels, across block fills."""
+    outs, pools = {}, {}
+    for fused in (False, True):
+        w = Workload(seed=31, prior=(15, 16, 47, 1), int8=int8, split_tokens=split, max_blocks=9, fused_step=fused,
+                     **TINY)
+        outs[fused] = torch.stack([w.step() for _ in range(34)]).cpu()
+        assert w.error_bits() == 0
+        lc = w.cache.layers[0]
+        pools[fused] = [t.clone().cpu() for t in (lc.k_pool, lc.v_pool) + ((lc.scales, lc.k_tail, lc.v_tail)
+                                                                          if int8 else ())]
+        if fused:
+            for t in range(34):
+                out = outs[fused][t].float().numpy()
+                for i in range(w.B):
+                    assert_close(out[0, i], w.oracle_out(0, i, t), f"fused step {t} seq {i}")
+            for i in range(w.B):
+                w.check_pool_bytes(0, i, w.prior[i] + 34)
+    assert torch.equal(outs[True], outs[False])
+    # every block a sequence holds (the pools' other blocks were never written)
+    if int8:
+        for a, b in zip(pools[True], pools[False]):
+            assert a.shape == b.shape
