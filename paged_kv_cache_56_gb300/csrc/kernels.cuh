@@ -698,53 +698,92 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         }
     }
     if (SPLIT && p.ws_count) {
-        // Fused split-K merge: the last split of (b, kv head) to finish merges
-        // all of them (partials are read from L2, past this SM's L1).
+        // Fused split-K merge: the last split of (b, kv head) to arrive merges
+        // all of them. Partials are read through L2 (past this SM's L1).
         __shared__ int s_last;
         const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
         int32_t* cnt = p.ws_count + size_t(b) * p.Hkv + kvh;
-        __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = atomicAdd(cnt, 1) == ns - 1;
+        if (tid == 0) s_last = atom_add_acq_rel_gpu(cnt, 1) == ns - 1;
         __syncthreads();
         if (!s_last) return;
-        __threadfence();
-        // Online merge of the splits' states, 16 splits per batch of
-        // independent loads (partials are read from L2, past this SM's L1).
-        for (int e = tid; e < G * D; e += kThreads) {
-            const int h = e / D, dim = e % D;
-            const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
-            const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + hrow * p.max_splits * 2);
-            const float* o = p.ws_o + hrow * p.max_splits * D + dim;
-            float mm = -1e30f, L = 0.f, O = 0.f;
-            for (int q0 = 0; q0 < ns; q0 += 16) {
-                float2 v[16];
-                float ov[16];
+        constexpr int EPT = (G * D + kThreads - 1) / kThreads;  // output elements per thread
+        constexpr int QB = EPT >= 48 ? 1 : 48 / EPT;   // splits per batch of loads
+        float* wsm = reinterpret_cast<float*>(stages);  // [G][ns] weights, then [G] sums
+        const bool staged = size_t(G) * ns + G <= size_t(kWarps) * STAGES * T::kStageBytes / 4;
+        // first batch of partial outputs: issued before the weights are known
+        float ov[QB][EPT];
+        auto load_o = [&](int q0) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (q0 + u < ns) {
-                        v[u] = __ldcg(ml + q0 + u);
-                        ov[u] = __ldcg(o + size_t(q0 + u) * D);
-                    } else {
-                        v[u] = make_float2(-1e30f, 0.f);
-                        ov[u] = 0.f;
-                    }
+            for (int u = 0; u < QB; ++u)
+#pragma unroll
+                for (int i = 0; i < EPT; ++i) {
+                    const int e = tid + i * kThreads, h = e / D, dim = e % D;
+                    const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
+                    ov[u][i] = (q0 + u < ns && e < G * D)
+                                   ? __ldcg(p.ws_o + (hrow * p.max_splits + q0 + u) * D + dim) : 0.f;
                 }
-                float bm = mm;
+        };
+        load_o(0);
+        if (staged) {
+            for (int h = warp; h < G; h += kWarps) {
+                const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
+                const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + hrow * p.max_splits * 2);
+                float mm = -1e30f;
+                for (int q = lane; q < ns; q += 32) mm = fmaxf(mm, __ldcg(ml + q).x);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) bm = fmaxf(bm, v[u].x);
-                const float c = fast_exp2(mm - bm);
-                L *= c;
-                O *= c;
-                mm = bm;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float w = fast_exp2(v[u].x - mm);
-                    L += w * v[u].y;
-                    O += w * ov[u];
+                for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, off));
+                float L = 0.f;
+                for (int q = lane; q < ns; q += 32) {
+                    const float2 v = __ldcg(ml + q);
+                    const float c = fast_exp2(v.x - mm);
+                    wsm[h * ns + q] = c;
+                    L += c * v.y;
                 }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+                if (lane == 0) wsm[G * ns + h] = L;
             }
-            reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            __syncthreads();
+            float acc[EPT];
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
+            for (int q0 = 0; q0 < ns; q0 += QB) {
+                if (q0 > 0) load_o(q0);
+#pragma unroll
+                for (int u = 0; u < QB; ++u)
+#pragma unroll
+                    for (int i = 0; i < EPT; ++i) {
+                        const int e = tid + i * kThreads, h = e / D;
+                        if (q0 + u < ns && e < G * D) acc[i] += wsm[h * ns + q0 + u] * ov[u][i];
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int e = tid + i * kThreads, h = e / D, dim = e % D;
+                if (e >= G * D) continue;
+                const float L = wsm[G * ns + h];
+                reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G + h) * D + dim] =
+                    __float2bfloat16_rn(L > 0.f ? acc[i] / L : 0.f);
+            }
+        } else {
+            // very many splits: one online pass per element
+            for (int e = tid; e < G * D; e += kThreads) {
+                const int h = e / D, dim = e % D;
+                const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
+                const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + hrow * p.max_splits * 2);
+                const float* o = p.ws_o + hrow * p.max_splits * D + dim;
+                float mm = -1e30f, L = 0.f, O = 0.f;
+                for (int q = 0; q < ns; ++q) {
+                    const float2 v = __ldcg(ml + q);
+                    const float nm = fmaxf(mm, v.x);
+                    const float c = fast_exp2(mm - nm), w = fast_exp2(v.x - nm);
+                    L = L * c + w * v.y;
+                    O = O * c + w * __ldcg(o + size_t(q) * D);
+                    mm = nm;
+                }
+                reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            }
         }
         if (tid == 0) *cnt = 0;  // ready for the next call
     }

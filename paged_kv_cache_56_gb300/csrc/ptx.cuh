@@ -84,6 +84,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// Atomic add with acquire-release semantics at GPU scope: the CTA's earlier
+// writes (ordered before this thread by a CTA barrier) are visible to whoever
+// acquires the counter afterwards, and this thread sees theirs.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // ---- loads -----------------------------------------------------------------
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
