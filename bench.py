@@ -50,6 +50,11 @@ WORKLOADS = {
     "long_int8": dict(L=1, B=8, prior=32768, Hq=32, Hkv=8, d=128, bs=64, num_blocks=4200, int8=True,
                       head_scale=False, outliers=True, repeat=32,
                       desc="long-context split-K: 8 x 32768 ctx, Hq=32 Hkv=8 d=128, bs=64, INT8, 1 layer x32"),
+    "trace": dict(L=32, B=128, prior=0, Hq=32, Hkv=8, d=128, bs=16, num_blocks=8192, int8=True,
+                  head_scale=False, outliers=False, repeat=1, steps=200,
+                  desc="continuous-batching trace: 200 steps, <=128 running, Poisson(2) arrivals, prompts "
+                       "log-uniform [16,4096], outputs geometric mean 300, 200-token shared prefix, Hq=32 Hkv=8 "
+                       "d=128, bs=16, INT8, 32 layers"),
     "tiny": dict(L=1, B=4, prior=[1, 17, 33, 100], Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=True,
                  head_scale=False, outliers=False, repeat=1,
                  desc="tiny correctness case: 1 layer, ctx {1,17,33,100}, Hq=4 Hkv=2 d=64, bs=16"),
@@ -218,6 +223,46 @@ class Bench:
             gs.run_eager()
         self.cache.commit_step(self.reqs)
         return plan
+
+
+def run_trace(args, wl):
+    """The continuous-batching trace: the first `warmup` steps fill the
+    system, the next `steps` are timed. Only the decode kernels of each step
+    are inside the CUDA events (admission prefill is setup, not the path)."""
+    from paged_kv_cache_56_gb300 import pkv, synth
+    from paged_kv_cache_56_gb300.runtime import PagedKVCache
+    from paged_kv_cache_56_gb300.trace import TraceDriver
+
+    pkv.pkv_set_programmatic_launch(not args.no_pdl)
+    total_steps = args.warmup + args.steps
+    bs = wl["bs"]
+    cache = PagedKVCache(wl["L"], wl["num_blocks"], wl["Hq"], wl["Hkv"], wl["d"], bs, wl["int8"],
+                         max_slots=wl["B"] + 1, max_blocks_per_seq=-(-(200 + 4096 + total_steps + 16) // bs),
+                         device=f"cuda:{torch.cuda.current_device()}",
+                         initial_order=synth.permutation(SEED, wl["num_blocks"]))
+    split = args.split if args.split is not None else 512
+    drv = TraceDriver(cache, SEED, total_steps, max_running=wl["B"], split_tokens=split)
+    for _ in range(args.warmup):
+        drv.step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs, nbytes, ntok, launches = [], 0, 0, 0
+    for _ in range(args.steps):
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        rids, plan = drv.step(events=ev)
+        if rids:
+            evs.append(ev)
+            nbytes += attention_bytes(plan.ctx_lens, wl["Hq"], wl["Hkv"], wl["d"], bs, wl["int8"]) * wl["L"]
+            ntok += len(rids)
+            launches += wl["L"]
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    if sum(lc.error_bits() for lc in cache.layers):
+        raise RuntimeError("device error bits set")
+    return dict(ms=ms, nbytes=nbytes, ntok=ntok, launches=launches, clocks=clk, split=split,
+                running=len(drv.running), finished=len(drv.finished))
 
 
 def run_device(args, wl, rank, world):
@@ -425,6 +470,23 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     from paged_kv_cache_56_gb300 import build as _build
     _build.build()
+    if args.workload == "trace":
+        r = run_trace(args, wl)
+        value = r["nbytes"] / (r["ms"] * 1e-3) / 1e9
+        line = {"metric": "paged decode-attention KV GB/s", "value": round(value, 2), "unit": "GB/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int8 KV / bf16 q,out / fp32 accumulate",
+                "data": "synthetic (seeded counter-based generator)",
+                "config": {"workload": "trace", "desc": wl["desc"], "split_tokens": r["split"],
+                           "timed": "decode kernels of each step (admission prefill excluded)",
+                           "running_at_end": r["running"], "finished": r["finished"]},
+                "tokens_per_s": round(r["ntok"] / (r["ms"] * 1e-3), 1),
+                "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
+                             "frac": round(value / peak, 4), "traffic": None, "peak_kind": peak_kind},
+                "clocks": r["clocks"], "gpu_launches": r["launches"], "e2e": None}
+        print(json.dumps(line), flush=True)
+        return
     r = run_device(args, wl, rank, world)
     if rank != 0:
         torch.distributed.destroy_process_group()

@@ -32,7 +32,10 @@
 
 namespace pkv {
 
-constexpr int kWarps = 4;
+#ifndef PKV_WARPS
+#define PKV_WARPS 4  // warps per decode CTA
+#endif
+constexpr int kWarps = PKV_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;  // tokens per staged tile
 constexpr unsigned kFull = 0xFFFFFFFFu;
