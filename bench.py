@@ -62,6 +62,34 @@ WORKLOADS = {
 SEED = 1234
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA/C++ sources and the C header (what an ncu capture measured)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_56_gb300", "csrc", "*")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the decode kernel from the ncu
+    capture recorded in profiles/dram_traffic.json, or None when the kernel
+    sources have changed since that capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    ent = rec.get("workloads", {}).get(workload)
+    return None if ent is None else int(ent["dram_bytes_per_launch"])
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -167,6 +195,10 @@ class Bench:
         self.reqs = list(range(1000, 1000 + B))
         self.sm_scale = 1.0 / math.sqrt(d)
         max_blocks = -(-(max(prior) + steps_total + 1) // bs)
+        need = sum(-(-(n + steps_total + 1) // bs) for n in prior)
+        if need > wl["num_blocks"]:
+            raise SystemExit(f"{steps_total} decode steps need {need} blocks per layer; the workload's pool "
+                             f"holds {wl['num_blocks']} (reduce --steps / --warmup / --e2e-steps)")
         self.cache = PagedKVCache(L, wl["num_blocks"], Hq, Hkv, d, bs, wl["int8"], max_slots=B,
                                   max_blocks_per_seq=max_blocks, device=device,
                                   initial_order=synth.permutation(SEED, wl["num_blocks"]))
@@ -431,9 +463,9 @@ def oracle_sample(wl, steps: int, budget_s: float = 20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="tts_talker", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -510,7 +542,8 @@ def main():
         "tokens_per_s": round(wl["B"] * world / (ms_step * 1e-3), 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.workload),
+                     "peak_kind": peak_kind,
                      "kernel": "decode_kernel via pkv_decode_step (append + quantize-on-fill + attention + split-K merge)",
                      "bytes_per_launch": int(r["attn_bytes"]), "avg_launch_us": round(attn_avg_ms * 1e3, 2),
                      "timing": "CUDA events over back-to-back replays of the step's kernels"},
