@@ -106,3 +106,18 @@ def test_fused_step_equals_separate_kernels(int8, split):
     if int8:
         for a, b in zip(pools[True], pools[False]):
             assert a.shape == b.shape
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+@pytest.mark.parametrize("max_blocks", [9, 24], ids=["9_splits", "24_splits"])
+def test_fused_merge_many_splits_match_oracle(int8, max_blocks):
+    """The fused split-K merge with few and with many splits per sequence,
+    empty splits (short sequences) in the mix, against the oracle."""
+    prior = (120, 3, 60, 17) if max_blocks == 9 else (360, 3, 60, 17)
+    w = Workload(seed=77, prior=prior, int8=int8, split_tokens=16, max_blocks=max_blocks, **TINY)
+    assert (w.bufs.max_splits <= 16) == (max_blocks == 9)
+    for t in range(6):
+        out = w.step().float().cpu().numpy()
+        for i in range(w.B):
+            assert_close(out[0, i], w.oracle_out(0, i, t), f"step {t} seq {i}")
+    assert w.error_bits() == 0
