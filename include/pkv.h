@@ -226,6 +226,21 @@ int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, c
                     int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count, void* out,
                     void* stream);
 
+/* A whole decode step over num_layers layers in one call, layer l after
+ * layer l-1 on the stream: layer l runs pkv_decode_step on descs[l] with
+ * q + l*q_layer_stride, k_new/v_new + l*kv_layer_stride and
+ * out + l*out_layer_stride (strides in bytes, multiples of 16), or
+ * pkv_decode_attention when k_new and v_new are both NULL. The block tables,
+ * context lengths, slots, split settings and workspace are shared by all
+ * layers (the layers of a model allocate the same blocks). Stops at, and
+ * returns, the first error. */
+int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const void* q,
+                      int64_t q_layer_stride, const void* k_new, const void* v_new,
+                      int64_t kv_layer_stride, void* out, int64_t out_layer_stride,
+                      const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                      const int32_t* slots, int32_t B, float sm_scale, int32_t split_tokens,
+                      int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count, void* stream);
+
 /* CTAs of the decode kernel for this cache shape that fit on one SM at once
  * (registers and shared memory), for a given split_tokens (0 = none) and
  * max_blocks; a caller sizes its splits so that B * Hkv * splits fills

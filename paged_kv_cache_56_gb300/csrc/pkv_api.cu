@@ -410,6 +410,29 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
                        max_splits, ws_o, ws_ml, ws_count, out, stream);
 }
 
+int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const void* q, int64_t q_layer_stride,
+                      const void* k_new, const void* v_new, int64_t kv_layer_stride, void* out,
+                      int64_t out_layer_stride, const int32_t* block_tables, int32_t max_blocks,
+                      const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
+                      int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count,
+                      void* stream) {
+    if (!descs || num_layers < 0 || !q || !out) return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if ((q_layer_stride | out_layer_stride | (k_new ? kv_layer_stride : 0)) & 15) return PKV_ERR_INVALID;
+    const auto* qb = static_cast<const uint8_t*>(q);
+    const auto* kb = static_cast<const uint8_t*>(k_new);
+    const auto* vb = static_cast<const uint8_t*>(v_new);
+    auto* ob = static_cast<uint8_t*>(out);
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const int rc = decode_impl(descs + l, qb + l * q_layer_stride, kb ? kb + l * kv_layer_stride : nullptr,
+                                   vb ? vb + l * kv_layer_stride : nullptr, block_tables, max_blocks, ctx_lens, slots,
+                                   B, sm_scale, split_tokens, max_splits, ws_o, ws_ml, ws_count,
+                                   ob + l * out_layer_stride, stream);
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
+}
+
 int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
                     const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                     int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml,

@@ -49,7 +49,7 @@ EXPORTED = (
     "pkv_build_block_tables", "pkv_append_kv", "pkv_quantize_full_blocks",
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
-    "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step",
+    "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step", "pkv_decode_layers",
 )
 
 
@@ -104,6 +104,9 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
             "pkv_set_programmatic_launch": (ctypes.c_int, [ctypes.c_int]),
+            "pkv_decode_layers": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _VP, _I64, _VP, _VP, _I64, _VP,
+                                                 _I64, _VP, _I32, _VP, _VP, _I32, ctypes.c_float, _I32, _I32, _VP,
+                                                 _VP, _VP, _VP]),
             "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _I32,
                                                ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_attention_static_ws": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP, _VP,
@@ -335,6 +338,68 @@ def pkv_decode_step(desc: CacheDesc, q: torch.Tensor, k_new: torch.Tensor, v_new
     _check("pkv_decode_step",
            lib().pkv_decode_step(_desc_ptr(desc), qp, kp, vp, tp, max_blocks, cp, sp, B, float(sm_scale),
                                  split_tokens, max_splits, wo, wml, wc, outp, _stream(stream)))
+
+
+def _layered(t: torch.Tensor, name: str, L: int, inner) -> int:
+    """Device pointer of a [>=L, *inner] bf16 tensor whose per-layer slices are
+    contiguous (the layer stride may exceed the slice, e.g. a batch slice of a
+    larger buffer); checks that every slice lies inside the storage."""
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    if t.dim() != 1 + len(inner) or t.shape[0] < L or tuple(t.shape[1:]) != tuple(inner):
+        raise ValueError(f"{name} must be [{L}, {', '.join(map(str, inner))}], got {tuple(t.shape)}")
+    n = 1
+    for x in inner:
+        n *= x
+    if not t[0].is_contiguous() or t.stride(0) < n:
+        raise ValueError(f"{name}: each layer's slice must be contiguous")
+    span = (L - 1) * t.stride(0) + n
+    avail = t.untyped_storage().nbytes() // 2 - t.storage_offset()
+    if span > avail:
+        raise ValueError(f"{name} does not hold {L} layers")
+    return t.data_ptr()
+
+
+def desc_array(descs) -> ctypes.Array:
+    """A contiguous C array of descriptors (one per layer) for pkv_decode_layers."""
+    arr = (CacheDesc * len(descs))()
+    for i, d in enumerate(descs):
+        ctypes.memmove(ctypes.byref(arr, i * ctypes.sizeof(CacheDesc)), ctypes.byref(d), ctypes.sizeof(CacheDesc))
+    return arr
+
+
+def pkv_decode_layers(descs: ctypes.Array, q: torch.Tensor, k_new, v_new, block_tables: torch.Tensor,
+                      ctx_lens: torch.Tensor, slots, sm_scale: float, out: torch.Tensor, split_tokens: int = 0,
+                      max_splits: int = 0, ws_o=None, ws_ml=None, ws_count=None, stream=None) -> None:
+    """Decode step over all layers in one call. q, out: [L, B, Hq, d]; k_new,
+    v_new: [L, B, Hkv, d] or None (attention only); descs from desc_array()."""
+    L = len(descs)
+    B = ctx_lens.numel()
+    d0 = descs[0]
+    hq, hkv, d = d0.num_q_heads, d0.num_kv_heads, d0.head_dim
+    qp = _layered(q, "q", L, (B, hq, d))
+    outp = _layered(out, "out", L, (B, hq, d))
+    kp = vp = None
+    kv_stride = 0
+    if k_new is not None:
+        if v_new is None or v_new.stride(0) != k_new.stride(0):
+            raise ValueError("k_new and v_new must be given together, with the same layer stride")
+        kp = _layered(k_new, "k_new", L, (B, hkv, d))
+        vp = _layered(v_new, "v_new", L, (B, hkv, d))
+        kv_stride = k_new.stride(0) * 2
+    max_blocks = block_tables.shape[-1] if block_tables.dim() == 2 else 0
+    tp = _dev(block_tables, "block_tables", torch.int32, B * max_blocks)
+    cp = _dev(ctx_lens, "ctx_lens", torch.int32, B)
+    sp = _opt_dev(slots, "slots", torch.int32, B)
+    wo = wml = wc = None
+    if split_tokens > 0:
+        wo = _dev(ws_o, "ws_o", torch.float32, B * hq * max_splits * d)
+        wml = _dev(ws_ml, "ws_ml", torch.float32, B * hq * max_splits * 2)
+        wc = _opt_dev(ws_count, "ws_count", torch.int32, B * hkv)
+    _check("pkv_decode_layers",
+           lib().pkv_decode_layers(descs, L, qp, q.stride(0) * 2, kp, vp, kv_stride, outp, out.stride(0) * 2, tp,
+                                   max_blocks, cp, sp, B, float(sm_scale), split_tokens, max_splits, wo, wml, wc,
+                                   _stream(stream)))
 
 
 def pkv_splitk_reduce(ws_o: torch.Tensor, ws_ml: torch.Tensor, ctx_lens: torch.Tensor, num_q_heads: int,

@@ -71,6 +71,7 @@ class TraceDriver:
                                device=cache.device)
         self.prefix_ids = []
         self._write_prefix()
+        self.descs = pkv.desc_array([lc.desc for lc in cache.layers])
 
     # -- synthetic rows ------------------------------------------------------
     def rows(self, layer: int, kind: int, rid: int, positions, device=None) -> torch.Tensor:
@@ -160,6 +161,21 @@ class TraceDriver:
         b = self.bufs
         inputs = [(self.q_rows(li, rids, self.step_no), self._new_rows(li, synth.KIND_K, rids, pos),
                    self._new_rows(li, synth.KIND_V, rids, pos)) for li in range(c.L)]
+        if self.fused:  # the whole step in one native call
+            qs = torch.stack([x[0] for x in inputs])
+            ks = torch.stack([x[1] for x in inputs])
+            vs = torch.stack([x[2] for x in inputs])
+            if events is not None:
+                events[0].record()
+            pkv.pkv_decode_layers(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
+                                  self.out[:, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
+            if events is not None:
+                events[1].record()
+            c.commit_step(rids)
+            for r in self.running:
+                r.generated += 1
+            self.step_no += 1
+            return rids, plan
         if events is not None:
             events[0].record()
         for li, lc in enumerate(c.layers):

@@ -121,3 +121,34 @@ def test_fused_merge_many_splits_match_oracle(int8, max_blocks):
         for i in range(w.B):
             assert_close(out[0, i], w.oracle_out(0, i, t), f"step {t} seq {i}")
     assert w.error_bits() == 0
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_decode_layers_equals_per_layer_steps(int8):
+    """pkv_decode_layers (one call for all layers) == pkv_decode_step per layer."""
+    from paged_kv_cache_56_gb300 import pkv, synth
+    outs = {}
+    for one_call in (False, True):
+        w = Workload(seed=8, num_layers=3, prior=(40, 17, 100, 1), Hq=4, Hkv=2, d=64, bs=16, num_blocks=96,
+                     int8=int8, split_tokens=32, max_blocks=9, fused_step=True)
+        res = []
+        for t in range(18):
+            if not one_call:
+                res.append(w.step().cpu())
+                continue
+            plan = w.cache.plan_step(w.req_ids)
+            w.bufs.upload(plan)
+            b, B = w.bufs, w.B
+            pos = torch.tensor(plan.positions, dtype=torch.int64)
+            q = torch.stack([w.q(li, t, w.req_ids) for li in range(3)])
+            k = torch.stack([w.kv(li, synth.KIND_K, w.req_ids, pos) for li in range(3)])
+            v = torch.stack([w.kv(li, synth.KIND_V, w.req_ids, pos) for li in range(3)])
+            out = torch.empty((3, 6, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")  # wider than the batch
+            pkv.pkv_decode_layers(pkv.desc_array([lc.desc for lc in w.cache.layers]), q, k, v, b.tab[:B],
+                                  b.ctx[:B], b.slot[:B], w.sm_scale, out[:, :B], b.split_tokens, b.max_splits,
+                                  b.ws_o, b.ws_ml, b.ws_count)
+            w.cache.commit_step(w.req_ids)
+            res.append(out[:, :B].cpu())
+        assert w.error_bits() == 0
+        outs[one_call] = torch.stack(res)
+    assert torch.equal(outs[True], outs[False])
