@@ -272,7 +272,7 @@ def run_trace(args, wl):
                          max_slots=wl["B"] + 1, max_blocks_per_seq=-(-(200 + 4096 + total_steps + 16) // bs),
                          device=f"cuda:{torch.cuda.current_device()}",
                          initial_order=synth.permutation(SEED, wl["num_blocks"]))
-    split = args.split if args.split is not None else 512
+    split = args.split if args.split is not None else 1536  # measured best at this workload (512..4096 swept)
     drv = TraceDriver(cache, SEED, total_steps, max_running=wl["B"], split_tokens=split)
     for _ in range(args.warmup):
         drv.step()

@@ -202,7 +202,9 @@ int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const v
  *   same stream. ws_count non-NULL: device int32 [B][Hkv], all zero before
  *   the first call; the last split of each (b, kv_head) to finish merges in
  *   the same kernel and sets its counter back to zero, so the array stays
- *   ready for the next call. Calls sharing a workspace must not overlap.
+ *   ready for the next call (a sequence whose context fits one split writes
+ *   its output directly, leaving workspace and counter untouched). Calls
+ *   sharing a workspace must not overlap.
  * slots may be NULL in BF16 mode. */
 int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
                          int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,

@@ -82,13 +82,11 @@ struct DecodeTraits {
 };
 
 // Shared-memory bytes of a decode CTA before its block table.
-template <int D, int G, bool INT8>
+template <int D, bool INT8>
 constexpr size_t decode_smem_fixed() {
     using T = DecodeTraits<D, INT8>;
-    return size_t(kWarps) * T::kStages * T::kStageBytes   // stages
-         + size_t(kWarps) * T::kStages * 8                // mbarriers
-         + size_t(kWarps) * G * D * 4                     // merge: o
-         + size_t(kWarps) * G * 2 * 4;                    // merge: m, l
+    return size_t(kWarps) * T::kStages * T::kStageBytes   // stages (and, after the loop, the merge)
+         + size_t(kWarps) * T::kStages * 8;               // mbarriers
 }
 
 // ---- tensor-core tile math ---------------------------------------------------
@@ -314,24 +312,31 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
     }
 }
 
-// Q^T fragments of head g (zero for g >= G): dims t*D/4 + 4ks + {0,1} and
-// {2,3} of the query row. F16: the row is scaled by 2^e (e per head, chosen so
-// that max|q| * 2^e lies in [2^14, 2^15) -- exact, and safe from f16
-// overflow); returns e. BF16: the raw row, e = 0.
-template <int D, int G, bool F16>
-__device__ __forceinline__ int load_q_frags(const uint16_t* qrow, int g, int t, uint32_t (&qf)[D / 16][2]) {
+// The query words behind a lane's Q^T fragments (head g, zero for g >= G):
+// dims t*D/4 .. t*D/4 + D/4 - 1 of the query row, read through L2 (the row is
+// written by the kernel this one waits for).
+template <int D, int G>
+__device__ __forceinline__ void load_q_words(const uint16_t* qrow, int g, int t, uint32_t (&w)[D / 8]) {
     constexpr int NW = D / 8;  // bf16 words in a lane's D/4 dims
-    uint32_t w[NW];
     if (g < G) {
 #pragma unroll
         for (int c = 0; c < NW / 4; ++c) {
-            const uint4 v = ldg128(qrow + t * (D / 4) + c * 8);
+            const uint4 v = ldcg128(qrow + t * (D / 4) + c * 8);
             w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
         }
     } else {
 #pragma unroll
         for (int i = 0; i < NW; ++i) w[i] = 0u;
     }
+}
+
+// Q^T fragments from the words of load_q_words: dims t*D/4 + 4ks + {0,1} and
+// {2,3} of the query row. F16: the row is scaled by 2^e (e per head, chosen so
+// that max|q| * 2^e lies in [2^14, 2^15) -- exact, and safe from f16
+// overflow); returns e. BF16: the raw row, e = 0.
+template <int D, bool F16>
+__device__ __forceinline__ int q_frags(const uint32_t (&w)[D / 8], uint32_t (&qf)[D / 16][2]) {
+    constexpr int NW = D / 8;
     if (!F16) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -433,10 +438,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
-    float* mo = reinterpret_cast<float*>(bars + kWarps * STAGES);
-    float* mml = mo + kWarps * G * D;
-    int32_t* tab = reinterpret_cast<int32_t*>(mml + kWarps * G * 2);
+    int32_t* tab = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
     float2* bsc = reinterpret_cast<float2*>(tab + p.tab_cap);
+    // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2] sit in its own
+    // ring, free once its last tile has been consumed.
+    static_assert(G * D * 4 + G * 8 <= STAGES * T::kStageBytes, "merge space fits one warp's ring");
+    auto mo_of = [&](int w) { return reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes); };
+    auto mml_of = [&](int w) { return mo_of(w) + G * D; };
 
     const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -501,12 +509,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
         bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
     };
+    // block scales, copied asynchronously (waited for before the main loop)
     auto load_scales = [&](int lo, int hi) {
         for (int i = lo + tid; i < hi; i += kThreads) {
             const int id = tab[i];
-            float2 sc = make_float2(0.f, 0.f);
-            if (id >= 0) sc = __ldcg(reinterpret_cast<const float2*>(p.scales + (size_t(id) * p.Hkv + kvh) * 2));
-            bsc[i] = sc;
+            if (id >= 0)
+                cp_async8(smem_addr(bsc + i), p.scales + (size_t(id) * p.Hkv + kvh) * 2);
+            else
+                bsc[i] = make_float2(0.f, 0.f);
         }
     };
     if (lane == 0)
@@ -517,6 +527,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     if (INT8) load_scales(0, nblk_stable);
 
     pdl_wait();  // the previous kernel (and so the previous layer) has completed
+
+    // the query: loaded first, so that its latency overlaps the update below
+    const uint16_t* qbase = p.q + (size_t(b) * p.Hq + size_t(kvh) * G) * D;
+    uint32_t qw[D / 8];
+    load_q_words<D, G>(qbase + size_t(g) * D, g, t, qw);
 
     // ---- fused step update: the split holding token ctx-1 writes that token's
     // K/V row (given in k_new / v_new) and, in INT8 mode, quantizes its block if
@@ -568,20 +583,48 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         }
     if (INT8) load_scales(nblk_stable, nblk);
 
-    const uint16_t* qbase = p.q + (size_t(b) * p.Hq + size_t(kvh) * G) * D;
+    WarpState<D> st;
+    st.m[0] = st.m[1] = -1e30f;
+    st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m) st.acc[m][0] = st.acc[m][1] = st.acc[m][2] = st.acc[m][3] = 0.f;
+
+    // ---- INT8: the partly filled last block, read from the bf16 tail -----------
+    // Done before the pool tiles: its global loads then overlap the ring's
+    // first bulk copies instead of following the last one. Tail tile tt goes to
+    // warp kWarps-1-tt, the warps with the fewest pool tiles.
+    if (INT8) {
+        const int tail_lo = max(t0, nfull);
+        const int ntail = t1 - tail_lo;
+        if (ntail > 0) {
+            const int slot = p.slots ? p.slots[b] : -1;
+            if (slot < 0 || slot >= p.max_slots) {
+                if (tid == 0) report(p.err, kErrSlot);
+            } else {
+                uint32_t qb[D / 16][2];
+                (void)q_frags<D, false>(qw, qb);
+                const float hb[2] = {p.qscale, p.qscale};
+                const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull);
+                const uint8_t* kt = static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2;
+                const uint8_t* vt = static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2;
+                for (int tt = kWarps - 1 - warp; tt * kTile < ntail; tt += kWarps) {
+                    const GmemRows kr{kt + size_t(tt) * kTile * D * 2, D * 2};
+                    const GmemRows vr{vt + size_t(tt) * kTile * D * 2, D * 2};
+                    mma_tile<D, false>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, qb, hb, g, t, st);
+                }
+            }
+        }
+    }
+
     uint32_t qf[D / 16][2];
-    const int qe = load_q_frags<D, G, INT8>(qbase + size_t(g) * D, g, t, qf);
+    const int qe = q_frags<D, INT8>(qw, qf);
     float hs[2];
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
         const int eh = __shfl_sync(kFull, qe, ((2 * t + jj) & 7) * 4);
         hs[jj] = p.qscale * ldexpf(1.0f, -eh);
     }
-    WarpState<D> st;
-    st.m[0] = st.m[1] = -1e30f;
-    st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-    for (int m = 0; m < D / 16; ++m) st.acc[m][0] = st.acc[m][1] = st.acc[m][2] = st.acc[m][3] = 0.f;
+    if (INT8) cp_async_wait_all();  // this thread's scale copies
     __syncthreads();
 
     // ---- main loop over this warp's pool tiles ----------------------------------
@@ -620,30 +663,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             (void)wait_phase(bar_of(kk % STAGES), uint32_t(kk / STAGES) & 1u);
     }
 
-    // ---- INT8: the partly filled last block is read from the bf16 tail -------
-    if (INT8) {
-        const int tail_lo = max(t0, nfull);
-        const int ntail = t1 - tail_lo;
-        if (ntail > 0) {
-            const int slot = p.slots ? p.slots[b] : -1;
-            if (slot < 0 || slot >= p.max_slots) {
-                if (tid == 0) report(p.err, kErrSlot);
-            } else {
-                uint32_t qb[D / 16][2];
-                (void)load_q_frags<D, G, false>(qbase + size_t(g) * D, g, t, qb);
-                const float hb[2] = {p.qscale, p.qscale};
-                const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull);
-                const uint8_t* kt = static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2;
-                const uint8_t* vt = static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2;
-                for (int tt = warp; tt * kTile < ntail; tt += kWarps) {
-                    const GmemRows kr{kt + size_t(tt) * kTile * D * 2, D * 2};
-                    const GmemRows vr{vt + size_t(tt) * kTile * D * 2, D * 2};
-                    mma_tile<D, false>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, qb, hb, g, t, st);
-                }
-            }
-        }
-    }
-
     // ---- merge: lanes of a warp hold disjoint dims; sum l over the 8 g lanes
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -654,15 +673,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     for (int jj = 0; jj < 2; ++jj) {
         const int h = 2 * t + jj;
         if (h < G) {
-            float* dst = mo + (warp * G + h) * D + g * (D / 8);
+            float* dst = mo_of(warp) + h * D + g * (D / 8);
 #pragma unroll
             for (int m = 0; m < D / 16; ++m) {
                 dst[2 * m] = st.acc[m][jj];
                 dst[2 * m + 1] = st.acc[m][2 + jj];
             }
             if (g == 0) {
-                mml[(warp * G + h) * 2] = st.m[jj];
-                mml[(warp * G + h) * 2 + 1] = st.l[jj];
+                mml_of(warp)[h * 2] = st.m[jj];
+                mml_of(warp)[h * 2 + 1] = st.l[jj];
             }
         }
     }
@@ -675,20 +694,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G) * D + e] = __float2bfloat16_rn(0.f);
         return;
     }
+    // With the fused merge, a sequence whose context fits one split has
+    // nothing to merge: its only split writes the output itself.
+    const int ns = SPLIT ? (ctx + p.split_tokens - 1) / p.split_tokens : 1;
+    const bool partial = SPLIT && !(p.ws_count && ns == 1);
     for (int e = tid; e < G * D; e += kThreads) {
         const int h = e / D, dim = e % D;
         float mm = -1e30f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, mml[(w * G + h) * 2]);
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, mml_of(w)[h * 2]);
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float c = fast_exp2(mml[(w * G + h) * 2] - mm);
-            L += mml[(w * G + h) * 2 + 1] * c;
-            O += mo[(w * G + h) * D + dim] * c;
+            const float c = fast_exp2(mml_of(w)[h * 2] - mm);
+            L += mml_of(w)[h * 2 + 1] * c;
+            O += mo_of(w)[h * D + dim] * c;
         }
         const size_t hrow = size_t(b) * p.Hq + kvh * G + h;
-        if (SPLIT) {
+        if (partial) {
             const size_t w = hrow * p.max_splits + j;
             p.ws_o[w * D + dim] = O;
             if (dim == 0) {
@@ -700,11 +723,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
             reinterpret_cast<__nv_bfloat16*>(p.out)[hrow * D + dim] = __float2bfloat16_rn(r);
         }
     }
-    if (SPLIT && p.ws_count) {
+    if (partial && p.ws_count) {
         // Fused split-K merge: the last split of (b, kv head) to arrive merges
         // all of them. Partials are read through L2 (past this SM's L1).
         __shared__ int s_last;
-        const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
         int32_t* cnt = p.ws_count + size_t(b) * p.Hkv + kvh;
         __syncthreads();
         if (tid == 0) s_last = atom_add_acq_rel_gpu(cnt, 1) == ns - 1;

@@ -192,18 +192,21 @@ static int allow_smem(DecodeFn fn, int index, size_t smem) {
         if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem)) != cudaSuccess)
             return PKV_ERR_CUDA;
+        // all of the unified L1 as shared memory: the kernel streams through
+        // shared memory and gains nothing from L1, and a smaller carveout
+        // would cap the CTAs per SM below what registers allow
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return PKV_ERR_CUDA;
         configured[index][dev] = int(smem);
     }
     return PKV_OK;
 }
 
-static size_t decode_smem(int d, int g, bool int8, int tab_cap) {
+static size_t decode_smem(int d, bool int8, int tab_cap) {
     size_t fixed = 0;
-    const size_t gd = size_t(g);
-    if (d == 64) fixed = int8 ? decode_smem_fixed<64, 1, true>() : decode_smem_fixed<64, 1, false>();
-    else fixed = int8 ? decode_smem_fixed<128, 1, true>() : decode_smem_fixed<128, 1, false>();
-    // decode_smem_fixed<.., G=1, ..> counts one head of merge space; add the rest
-    fixed += size_t(kWarps) * (gd - 1) * (size_t(d) * 4 + 8);
+    if (d == 64) fixed = int8 ? decode_smem_fixed<64, true>() : decode_smem_fixed<64, false>();
+    else fixed = int8 ? decode_smem_fixed<128, true>() : decode_smem_fixed<128, false>();
     return fixed + size_t(tab_cap) * (int8 ? 12 : 4);
 }
 
@@ -324,7 +327,7 @@ int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_
     if (split_tokens > 0 && (split_tokens % c->block_size || split_tokens % kTile)) return PKV_ERR_INVALID;
     const bool int8 = c->dtype == PKV_DTYPE_INT8;
     const int g = c->num_q_heads / c->num_kv_heads;
-    const size_t smem = decode_smem(c->head_dim, g, int8, decode_tab_cap(c, split_tokens, max_blocks));
+    const size_t smem = decode_smem(c->head_dim, int8, decode_tab_cap(c, split_tokens, max_blocks));
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
     int index = 0;
     DecodeFn fn = pick_decode(c->head_dim, g, int8, split_tokens > 0, &index);
@@ -358,7 +361,7 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     if (split && ws_count && (reinterpret_cast<uintptr_t>(ws_count) & 3u)) return PKV_ERR_INVALID;
     const int g = c->num_q_heads / c->num_kv_heads;
     const int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
-    const size_t smem = decode_smem(c->head_dim, g, int8, tab_cap);
+    const size_t smem = decode_smem(c->head_dim, int8, tab_cap);
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
     DecodeParams p;

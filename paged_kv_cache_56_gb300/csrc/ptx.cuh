@@ -127,6 +127,12 @@ __device__ __forceinline__ uint4 ldg128(const void* p) {
     return v;
 }
 
+// Asynchronous 8-byte global -> shared copy (completion: cp_async_wait_all).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- conversions -------------------------------------------------------------
 // Two bf16 in one word -> fp32 (exact: a bf16 is the top half of an fp32).
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {

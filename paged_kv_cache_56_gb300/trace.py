@@ -153,7 +153,9 @@ class TraceDriver:
         if not self.running:
             self.step_no += 1
             return [], None
-        rids = [r.rid for r in self.running]
+        # longest context first: the grid runs its CTAs in batch order, so the
+        # longest sequences start first and the short ones fill in behind them
+        rids = [r.rid for r in sorted(self.running, key=lambda r: -r.length)]
         plan = c.plan_step(rids)
         self.bufs.upload(plan)
         B = len(rids)
