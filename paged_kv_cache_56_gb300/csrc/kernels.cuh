@@ -37,6 +37,8 @@ namespace pkv {
 #endif
 constexpr int kWarps = PKV_WARPS;
 constexpr int kThreads = kWarps * 32;
+// decode CTAs kept resident per SM: 16 warps (the register file at 128 registers a thread)
+constexpr int kMinCtas = kWarps >= 16 ? 1 : 16 / kWarps;
 constexpr int kTile = 16;  // tokens per staged tile
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -430,7 +432,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
 }
 
 template <int D, int G, bool INT8, bool SPLIT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
     using T = DecodeTraits<D, INT8>;
     using Gm = Geom<D, INT8>;
@@ -560,13 +562,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         __syncthreads();
         if (INT8 && ok && (pos + 1) % p.bs == 0) {
             if (id >= 0) {
-                if (warp < 2) {
-                    const uint16_t* src = static_cast<const uint16_t*>(warp ? p.v_tail : p.k_tail) +
+                for (int kv = warp; kv < 2; kv += kWarps) {  // K slab, V slab
+                    const uint16_t* src = static_cast<const uint16_t*>(kv ? p.v_tail : p.k_tail) +
                                           (size_t(slot) * p.Hkv + kvh) * p.bs * D;
-                    int8_t* dst = static_cast<int8_t*>(const_cast<void*>(warp ? p.v_pool : p.k_pool)) +
+                    int8_t* dst = static_cast<int8_t*>(const_cast<void*>(kv ? p.v_pool : p.k_pool)) +
                                   (size_t(id) * p.Hkv + kvh) * p.bs * D;
                     quantize_slab<D, true>(lane, src, D, p.bs, dst,
-                                           const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + warp);
+                                           const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + kv);
                     fence_proxy_async_global();  // the codes are read by a bulk copy below
                 }
             } else if (tid == 0) {

@@ -152,3 +152,23 @@ def test_decode_layers_equals_per_layer_steps(int8):
         assert w.error_bits() == 0
         outs[one_call] = torch.stack(res)
     assert torch.equal(outs[True], outs[False])
+
+
+@pytest.mark.parametrize("split", [0, 32])
+def test_single_kv_head_odd_pool(split):
+    """INT8 with one kv head and an odd pool (63 blocks, scale entries at
+    every 8-byte offset): with this seed the pool's last block is a full block
+    of the fourth sequence, read through the pool every step, and the pool
+    ends the run fully held."""
+    w = Workload(seed=3, num_layers=1, prior=(224, 224, 224, 207), Hq=2, Hkv=1, d=64, bs=16, num_blocks=63,
+                 int8=True, split_tokens=split, max_blocks=17)
+    assert 62 in w.cache.table(w.req_ids[3])[: 207 // 16]
+    for t in range(20):  # ends with all 63 blocks held
+        out = w.step().float().cpu().numpy()
+        if t % 5 == 4:
+            for i in range(w.B):
+                assert_close(out[0, i], w.oracle_out(0, i, t), f"step {t} seq {i}")
+    assert max(max(w.cache.table(r)) for r in w.req_ids) == 62  # the last block is in use
+    assert w.error_bits() == 0
+    for i in range(w.B):
+        w.check_pool_bytes(0, i, w.prior[i] + 20)
