@@ -153,9 +153,7 @@ class TraceDriver:
         if not self.running:
             self.step_no += 1
             return [], None
-        # longest context first: the grid runs its CTAs in batch order, so the
-        # longest sequences start first and the short ones fill in behind them
-        rids = [r.rid for r in sorted(self.running, key=lambda r: -r.length)]
+        rids = self.batch_order()
         plan = c.plan_step(rids)
         self.bufs.upload(plan)
         B = len(rids)
@@ -199,6 +197,12 @@ class TraceDriver:
             r.generated += 1
         self.step_no += 1
         return rids, plan
+
+    def batch_order(self) -> list:
+        """Running request ids in the order the step batches them: longest
+        context first. The decode grid starts its CTAs in batch order, so the
+        longest sequences start first and the short ones fill in behind them."""
+        return [r.rid for r in sorted(self.running, key=lambda r: -r.length)]
 
     def _new_rows(self, layer: int, kind: int, rids, positions) -> torch.Tensor:
         c = self.cache
