@@ -297,6 +297,22 @@ def run_trace(args, wl):
                 running=len(drv.running), finished=len(drv.finished))
 
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The job's time: the slowest rank's timed region (every rank runs the
+    same number of steps on its own replica)."""
+    if world <= 1:
+        return ms
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed over the job's time."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def run_device(args, wl, rank, world):
     from paged_kv_cache_56_gb300.runtime import GraphStep
 
@@ -367,10 +383,7 @@ def run_device(args, wl, rank, world):
     clk = clocks.stop()
     attn_call_ms = a0.elapsed_time(a1) / (attn_reps * L * R)
     attn_bytes = attention_bytes(ctx_hist[-1], Hq, Hkv, d, bs, wl["int8"])
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     step_bytes = sum(attention_bytes(c, Hq, Hkv, d, bs, wl["int8"]) for c in ctx_hist) * L * R
     err = sum(lc.error_bits() for lc in bench.cache.layers)
     if err:
@@ -388,6 +401,8 @@ def run_device(args, wl, rank, world):
             host_in.append(tuple(t.cpu().pin_memory() for t in (q, k, v)))
         hout = torch.empty(gs.out.shape, dtype=gs.out.dtype).pin_memory()
         e_ctx = []
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record()
@@ -397,11 +412,11 @@ def run_device(args, wl, rank, world):
             e_ctx.append(plan.ctx_lens.copy())
         t1.record()
         torch.cuda.synchronize()
-        e_ms = t0.elapsed_time(t1)
+        e_ms = max_over_ranks(t0.elapsed_time(t1), world)
         e_bytes = sum(attention_bytes(c, Hq, Hkv, d, bs, wl["int8"]) for c in e_ctx) * L * R
         h2d = sum(t.numel() * t.element_size() for t in host_in[0])
-        e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "tokens_per_s": round(B * args.e2e_steps / (e_ms * 1e-3), 1),
+        e2e = {"value": round(job_gbs(e_bytes, world, e_ms), 2), "unit": "GB/s",
+               "tokens_per_s": round(B * world * args.e2e_steps / (e_ms * 1e-3), 1),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
                "ms_per_step": round(e_ms / args.e2e_steps, 4)}
     return dict(ms=ms, attn_call_ms=attn_call_ms, attn_bytes=attn_bytes, step_bytes=step_bytes, clocks=clk,
@@ -524,7 +539,7 @@ def main():
         torch.distributed.destroy_process_group()
         return
     ms_step = r["ms"] / args.steps
-    value = r["step_bytes"] * world / (r["ms"] * 1e-3) / 1e9
+    value = job_gbs(r["step_bytes"], world, r["ms"])
     attn_avg_ms = r["attn_call_ms"]
     achieved = r["attn_bytes"] / (attn_avg_ms * 1e-3) / 1e9
     line = {
