@@ -24,6 +24,21 @@ the design notes):
 * blocks shared by many requests (a common prompt prefix, [B] §3.2, [E] §2.1)
   are attached in front of a request's private blocks and are never returned
   by ``free`` -- whoever allocated them owns them.
+
+Copy-on-write forking ([B] §3.2: requests with a common prefix point at the
+same physical blocks, and a block is copied only when one of them must write
+into it -- parallel sampling, beam search):
+
+* ``fork(parent, child)`` gives the child the parent's whole table; every
+  block the parent holds is now held by both. A block's reference count is
+  the number of live requests whose own list holds it;
+* ``cow(req, i)`` is called before a request writes into its logical block i:
+  if that block is held by others too, the request takes a fresh block from
+  the front of the free list in its place (the caller copies the contents
+  over) and ``(old, new)`` is returned; a block held by the request alone
+  needs no copy (``None``). Attached prefix blocks are read-only;
+* ``free(req)`` drops the request's references and returns, in its order,
+  only the blocks nobody holds any more.
 """
 
 from __future__ import annotations
@@ -70,8 +85,9 @@ class FreeBlockPool:
     def free(self, req: int) -> list:
         if req not in self.private:
             raise UnknownRequest(req)
-        returned = self.private.pop(req)
+        held = self.private.pop(req)
         self.shared.pop(req)
+        returned = [b for b in held if self.refs(b) == 0]
         self.free_list.extend(returned)
         return returned
 
@@ -90,6 +106,36 @@ class FreeBlockPool:
         if req not in self.private:
             raise UnknownRequest(req)
         self.shared[req] = [int(b) for b in ids] + self.shared[req]
+
+    # -- copy-on-write forking ---------------------------------------------
+    def refs(self, block: int) -> int:
+        """Live requests whose own block list holds ``block``."""
+        return sum(block in held for held in self.private.values())
+
+    def fork(self, parent: int, child: int) -> None:
+        if parent not in self.private:
+            raise UnknownRequest(parent)
+        if child in self.private:
+            raise DuplicateRequest(child)
+        self.private[child] = list(self.private[parent])
+        self.shared[child] = list(self.shared[parent])
+
+    def cow(self, req: int, index: int):
+        """Before ``req`` writes into its logical block ``index``: None if the
+        block is its alone, else (old, new) after swapping in a fresh block."""
+        if req not in self.private:
+            raise UnknownRequest(req)
+        k = index - len(self.shared[req])
+        if k < 0:
+            raise ValueError("attached prefix blocks are read-only")
+        old = self.private[req][k]
+        if self.refs(old) <= 1:
+            return None
+        if not self.free_list:
+            raise OutOfBlocks(req)
+        new = self.free_list.pop(0)
+        self.private[req][k] = new
+        return old, new
 
     # -- views -------------------------------------------------------------
     def table(self, req: int) -> list:

@@ -8,11 +8,12 @@ import pytest
 from oracle.allocator import (FreeBlockPool, OutOfBlocks, UnknownRequest, DuplicateRequest)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "allocator_trace.txt")
+COW_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "cow_trace.txt")
 
 
-def _run_golden():
+def _run_golden(path=GOLDEN):
     pool = None
-    with open(GOLDEN) as f:
+    with open(path) as f:
         for line in f:
             line = line.split("#")[0].rstrip()
             if not line.strip():
@@ -131,3 +132,98 @@ def test_page_example_600_tokens():
     ids = pool.alloc("s", 38)
     assert len(ids) == 38 and pool.num_free() == 2048 - 38
     assert 38 * 16 - 600 == 8 < 16
+
+
+def test_cow_golden_trace():
+    n = 0
+    for pool, op, args, want in _run_golden(COW_GOLDEN):
+        n += 1
+        try:
+            if op == "alloc":
+                got = [str(b) for b in pool.alloc(args[0], int(args[1]))]
+            elif op == "append":
+                b = pool.append_block(args[0])
+                got = ["EMPTY"] if b is None else [str(b)]
+            elif op == "free":
+                got = [str(b) for b in pool.free(args[0])]
+            elif op == "fork":
+                pool.fork(args[0], args[1])
+                got = []
+            elif op == "cow":
+                r = pool.cow(args[0], int(args[1]))
+                got = ["NONE"] if r is None else [str(r[0]), str(r[1])]
+            elif op == "refs":
+                got = [str(pool.refs(int(args[0])))]
+            elif op == "free_list":
+                got = [str(b) for b in pool.free_list]
+            elif op == "table":
+                got = [str(b) for b in pool.table(args[0])]
+            else:
+                raise AssertionError(op)
+        except OutOfBlocks:
+            got = ["OOM"]
+        except DuplicateRequest:
+            got = ["DUP"]
+        except UnknownRequest:
+            got = ["UNKNOWN"]
+        assert got == want, (op, args, got)
+    assert n > 20
+
+
+def test_random_forks_keep_reference_counts():
+    """Random alloc / append / fork / cow / free: every block is free xor held,
+    a block's count is the number of requests holding it, a cow leaves the
+    writer's block held by it alone, and freeing everything restores the pool."""
+    rng = random.Random(11)
+    pool = FreeBlockPool(40, initial_order=rng.sample(range(40), 40))
+    live, nxt = [], 0
+    for _ in range(3000):
+        op = rng.random()
+        try:
+            if op < 0.2 or not live:
+                pool.alloc(nxt, rng.randint(0, 4))
+                live.append(nxt)
+                nxt += 1
+            elif op < 0.4:
+                pool.append_block(rng.choice(live))
+            elif op < 0.55:
+                pool.fork(rng.choice(live), nxt)
+                live.append(nxt)
+                nxt += 1
+            elif op < 0.8:
+                r = rng.choice(live)
+                t = pool.table(r)
+                if t:
+                    i = rng.randrange(len(t))
+                    before = pool.refs(t[i])
+                    res = pool.cow(r, i)
+                    t2 = pool.table(r)
+                    assert (res is None) == (before == 1)
+                    assert pool.refs(t2[i]) == 1
+                    if res is not None:
+                        assert res == (t[i], t2[i]) and pool.refs(t[i]) == before - 1
+            else:
+                r = rng.choice(live)
+                held = set(pool.table(r))
+                back = pool.free(r)
+                live.remove(r)
+                assert set(back) == {b for b in held if pool.refs(b) == 0}
+        except OutOfBlocks:
+            pass
+        held = {b for r in pool.private for b in pool.private[r]}
+        assert held.isdisjoint(pool.free_list)
+        assert sorted(held | set(pool.free_list)) == list(range(40))
+        assert len(pool.free_list) == len(set(pool.free_list))
+    for r in list(live):
+        pool.free(r)
+    assert sorted(pool.free_list) == list(range(40))
+
+
+def test_cow_of_attached_prefix_is_rejected():
+    pool = FreeBlockPool(8)
+    pool.alloc("prefix", 2)
+    pool.alloc("A", 1)
+    pool.attach_shared("A", [0, 1])
+    with pytest.raises(ValueError):
+        pool.cow("A", 1)
+    assert pool.cow("A", 2) is None
