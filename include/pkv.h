@@ -99,10 +99,38 @@ int pkv_alloc(pkv_allocator* a, int64_t req_id, int32_t n_blocks, int32_t* out_i
  * is empty ("wait"), PKV_ERR_NOT_FOUND for an unknown request. */
 int pkv_append_block(pkv_allocator* a, int64_t req_id, int32_t* out_id);
 
-/* Returns the request's private blocks to the back of the free list in the
- * order it held them and forgets the request ([D] §4.2 "free").
+/* Drops the request's hold on its blocks and forgets the request ([D] §4.2
+ * "free"): each block no other live request holds (see pkv_fork) goes to the
+ * back of the free list, in the order the request held them.
  * PKV_ERR_NOT_FOUND (no change) for an unknown request. */
 int pkv_free(pkv_allocator* a, int64_t req_id);
+
+/* Copy-on-write forking ([B] §3.2: requests sharing a prefix point at the
+ * same physical blocks, and a block is copied only when one of them needs to
+ * write into it -- parallel sampling, beam search). A block's reference count
+ * is the number of live requests holding it (1 after pkv_alloc or
+ * pkv_append_block).
+ *
+ * pkv_fork: new request `child` holds every block of live request `parent`
+ * (same table, pinned prefix included); each held block's count goes up by
+ * one. PKV_ERR_NOT_FOUND (parent), PKV_ERR_EXISTS (child); no change then. */
+int pkv_fork(pkv_allocator* a, int64_t parent, int64_t child);
+
+/* Before request req_id writes into its logical block `index`: if that block
+ * is also held by another request, a block from the front of the free list
+ * takes its place in req_id's table (the old block's count drops by one)
+ * and *out_src / *out_dst receive the old and new ids -- the caller copies
+ * the old block's contents into the new one (pkv_copy_blocks) before
+ * writing. A block held by req_id alone needs nothing: *out_src = *out_dst
+ * = -1. PKV_ERR_OOM if a copy is needed and the pool is empty (no change);
+ * PKV_ERR_INVALID for an index past the table or inside the pinned prefix
+ * (pkv_attach_shared blocks are read-only); PKV_ERR_NOT_FOUND for an unknown
+ * request. */
+int pkv_cow_block(pkv_allocator* a, int64_t req_id, int32_t index, int32_t* out_src, int32_t* out_dst);
+
+/* Reference count of a block (0 = free, or pinned-only); PKV_ERR_INVALID for
+ * an id outside the pool. */
+int pkv_block_refs(const pkv_allocator* a, int32_t block);
 
 /* Puts n shared block ids in front of a live request's table. They are
  * never returned by pkv_free; their owner (the request that allocated them)
@@ -180,6 +208,26 @@ int pkv_quantize_full_blocks(const pkv_cache_desc* c, const int32_t* block_ids,
  * INT8 mode only. */
 int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const void* v_src,
                              const int32_t* block_ids, int32_t M, void* stream);
+
+/* Copies whole pool blocks, src_ids[i] -> dst_ids[i] for i < n (device int32
+ * arrays): the K and V rows of every kv head and, INT8, the block's scales
+ * -- the copy half of copy-on-write ([B] §3.2; the ids come from
+ * pkv_cow_block). src_ids[i] < 0 or == dst_ids[i] is an entry with nothing
+ * to copy; another id outside [0, num_blocks) is skipped and reported
+ * (PKV_DEVERR_BLOCK_ID). Destinations must not overlap sources in flight.
+ * In INT8 mode a block that has not filled yet holds no pool data (its rows
+ * are in the slot's tail), so a write into a shared partial block needs the
+ * tail copied (pkv_copy_slots, at fork time) but no pool copy. */
+int pkv_copy_blocks(const pkv_cache_desc* c, const int32_t* src_ids, const int32_t* dst_ids, int32_t n,
+                    void* stream);
+
+/* INT8 mode: copies the bf16 tails of slots src_slots[i] -> dst_slots[i]
+ * (device int32, n entries; negative src = nothing to copy; other indices
+ * outside [0, max_slots) skipped and reported as PKV_DEVERR_SLOT) -- a
+ * forked request starts from its parent's partly filled block.
+ * PKV_ERR_INVALID in BF16 mode. */
+int pkv_copy_slots(const pkv_cache_desc* c, const int32_t* src_slots, const int32_t* dst_slots, int32_t n,
+                   void* stream);
 
 /* Decode attention ([B] §3.1 one new query against all cached K, V;
  * [E] §1 each decode step reads the whole cache; [A] §2 GQA; [C] §2 tiled

@@ -3,9 +3,14 @@
 // The pool is the free-block queue of "连续批处理与KV缓存" §4.2 (all free
 // blocks in one queue, taken from the front, returned at the back, O(1)
 // per block), stored as a fixed ring of num_blocks int32 so that no
-// operation moves the whole list. Requests own ordered lists of private
-// blocks and may reference shared blocks in front of them (a shared prompt
-// prefix: "vLLM核心概念" §3.2; "轻量级推理引擎实战" §2.1).
+// operation moves the whole list. Requests hold ordered lists of blocks and
+// may reference pinned shared blocks in front of them (a shared prompt
+// prefix: "vLLM核心概念" §3.2; "轻量级推理引擎实战" §2.1). A held block carries
+// a reference count -- the live requests holding it -- so that a request can
+// be forked (the child holds every block of the parent) and a block is
+// replaced by a private copy only when one holder writes into it
+// (copy-on-write, "vLLM核心概念" §3.2); free returns a block to the pool when
+// its last holder lets go.
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -20,9 +25,10 @@ struct pkv_allocator {
     std::vector<int32_t> ring;  // capacity num_blocks; free ids live in [head, head + count)
     int64_t head = 0;
     int64_t count = 0;
+    std::vector<int32_t> refs;  // per block: live requests holding it (0 = free or pinned-only)
     struct Request {
-        std::vector<int32_t> shared;
-        std::vector<int32_t> owned;
+        std::vector<int32_t> shared;  // pinned blocks, read-only, not counted
+        std::vector<int32_t> owned;   // held blocks, counted in refs
     };
     std::unordered_map<int64_t, Request> live;
 
@@ -30,6 +36,7 @@ struct pkv_allocator {
         int32_t id = ring[static_cast<size_t>(head)];
         head = (head + 1 == num_blocks) ? 0 : head + 1;
         --count;
+        refs[static_cast<size_t>(id)] = 1;
         return id;
     }
     void push_back(int32_t id) {
@@ -49,6 +56,7 @@ pkv_allocator* pkv_allocator_create(int32_t num_blocks, int32_t block_size,
     if (!a) return nullptr;
     try {
         a->ring.resize(static_cast<size_t>(num_blocks));
+        a->refs.assign(static_cast<size_t>(num_blocks), 0);
         if (initial_order) {
             std::vector<uint8_t> seen(static_cast<size_t>(num_blocks), 0);
             for (int32_t i = 0; i < num_blocks; ++i) {
@@ -115,7 +123,8 @@ int pkv_free(pkv_allocator* a, int64_t req_id) {
     if (!a) return PKV_ERR_INVALID;
     auto it = a->live.find(req_id);
     if (it == a->live.end()) return PKV_ERR_NOT_FOUND;
-    for (int32_t id : it->second.owned) a->push_back(id);
+    for (int32_t id : it->second.owned)
+        if (--a->refs[static_cast<size_t>(id)] == 0) a->push_back(id);
     a->live.erase(it);
     return PKV_OK;
 }
@@ -133,6 +142,47 @@ int pkv_attach_shared(pkv_allocator* a, int64_t req_id, const int32_t* ids, int3
         return PKV_ERR_OOM;
     }
     return PKV_OK;
+}
+
+int pkv_fork(pkv_allocator* a, int64_t parent, int64_t child) {
+    if (!a) return PKV_ERR_INVALID;
+    auto it = a->live.find(parent);
+    if (it == a->live.end()) return PKV_ERR_NOT_FOUND;
+    if (a->live.count(child)) return PKV_ERR_EXISTS;
+    try {
+        pkv_allocator::Request r = it->second;  // copies both lists
+        a->live.emplace(child, std::move(r));
+    } catch (...) {
+        return PKV_ERR_OOM;
+    }
+    for (int32_t id : a->live.find(child)->second.owned) ++a->refs[static_cast<size_t>(id)];
+    return PKV_OK;
+}
+
+int pkv_cow_block(pkv_allocator* a, int64_t req_id, int32_t index, int32_t* out_src, int32_t* out_dst) {
+    if (!a || !out_src || !out_dst || index < 0) return PKV_ERR_INVALID;
+    auto it = a->live.find(req_id);
+    if (it == a->live.end()) return PKV_ERR_NOT_FOUND;
+    auto& r = it->second;
+    const size_t ns = r.shared.size();
+    if (static_cast<size_t>(index) < ns) return PKV_ERR_INVALID;  // pinned blocks are read-only
+    const size_t k = static_cast<size_t>(index) - ns;
+    if (k >= r.owned.size()) return PKV_ERR_INVALID;
+    const int32_t old = r.owned[k];
+    *out_src = *out_dst = -1;
+    if (a->refs[static_cast<size_t>(old)] <= 1) return PKV_OK;  // held by this request alone
+    if (a->count == 0) return PKV_ERR_OOM;
+    const int32_t fresh = a->pop_front();
+    --a->refs[static_cast<size_t>(old)];
+    r.owned[k] = fresh;
+    *out_src = old;
+    *out_dst = fresh;
+    return PKV_OK;
+}
+
+int pkv_block_refs(const pkv_allocator* a, int32_t block) {
+    if (!a || block < 0 || block >= a->num_blocks) return PKV_ERR_INVALID;
+    return a->refs[static_cast<size_t>(block)];
 }
 
 int pkv_num_free(const pkv_allocator* a) { return a ? static_cast<int>(a->count) : -1; }

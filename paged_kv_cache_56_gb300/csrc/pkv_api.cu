@@ -138,6 +138,39 @@ static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK 
 
 static std::atomic<int> g_pdl{0};
 
+// Copies whole slabs src[i] -> dst[i] for up to three arrays at once (slab
+// index * slab bytes = offset; arrays may be NULL): a0 and a1 with slabs of
+// bytes01 (a multiple of 16) -- the K and V pools, or the K and V tails --
+// and a2 with slabs of bytes2 (a multiple of 8) -- the INT8 scales. One CTA
+// per pair; a negative src is a "nothing to copy" entry; an index outside
+// [0, limit) is skipped and reported.
+__global__ void __launch_bounds__(256) copy_slabs_kernel(const int32_t* __restrict__ src,
+                                                         const int32_t* __restrict__ dst, int32_t limit,
+                                                         uint8_t* a0, uint8_t* a1, size_t bytes01, uint8_t* a2,
+                                                         size_t bytes2, int32_t* err, int err_bit) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int i = blockIdx.x;
+    const int s = src[i], d = dst[i];
+    if (s < 0 || s == d) return;
+    if (s >= limit || d < 0 || d >= limit) {
+        if (threadIdx.x == 0) report(err, err_bit);
+        return;
+    }
+    uint8_t* arr[2] = {a0, a1};
+    for (int k = 0; k < 2; ++k) {
+        if (!arr[k]) continue;
+        const uint4* from = reinterpret_cast<const uint4*>(arr[k] + size_t(s) * bytes01);
+        uint4* to = reinterpret_cast<uint4*>(arr[k] + size_t(d) * bytes01);
+        for (size_t c = threadIdx.x; c < bytes01 / 16; c += blockDim.x) to[c] = from[c];
+    }
+    if (a2) {
+        const uint2* from = reinterpret_cast<const uint2*>(a2 + size_t(s) * bytes2);
+        uint2* to = reinterpret_cast<uint2*>(a2 + size_t(d) * bytes2);
+        for (size_t c = threadIdx.x; c < bytes2 / 8; c += blockDim.x) to[c] = from[c];
+    }
+}
+
 // Launches with the programmatic-stream-serialization attribute when enabled
 // (pkv_set_programmatic_launch), plainly otherwise.
 template <typename... Params, typename... Args>
@@ -289,6 +322,38 @@ int pkv_quantize_full_blocks(const pkv_cache_desc* c, const int32_t* block_ids, 
 int pkv_quantize_blocks_from(const pkv_cache_desc* c, const void* k_src, const void* v_src,
                              const int32_t* block_ids, int32_t M, void* stream) {
     return quantize_common(c, k_src, v_src, 0, block_ids, nullptr, M, stream);
+}
+
+static int copy_slabs(const pkv_cache_desc* c, bool slots, const int32_t* src, const int32_t* dst, int32_t n,
+                      void* stream) {
+    int st = check_desc(c);
+    if (st != PKV_OK) return st;
+    if (n < 0) return PKV_ERR_INVALID;
+    if (n == 0) return PKV_OK;
+    if (!src || !dst) return PKV_ERR_INVALID;
+    const bool int8 = c->dtype == PKV_DTYPE_INT8;
+    if (slots && !int8) return PKV_ERR_INVALID;
+    const size_t rows = size_t(c->num_kv_heads) * size_t(c->block_size) * size_t(c->head_dim);
+    auto s = static_cast<cudaStream_t>(stream);
+    if (slots)  // bf16 tails [slot][Hkv][bs][d]
+        return launch(copy_slabs_kernel, dim3(unsigned(n)), dim3(256), 0, s, src, dst, c->max_slots,
+                      static_cast<uint8_t*>(c->k_tail), static_cast<uint8_t*>(c->v_tail), rows * 2,
+                      static_cast<uint8_t*>(nullptr), size_t(0), c->err_word, int(kErrSlot));
+    // pool blocks [block][Hkv][bs][d] (+ INT8 scales [block][Hkv][2] fp32)
+    const size_t sc_bytes = int8 ? size_t(c->num_kv_heads) * 8 : 0;
+    return launch(copy_slabs_kernel, dim3(unsigned(n)), dim3(256), 0, s, src, dst, c->num_blocks,
+                  static_cast<uint8_t*>(c->k_pool), static_cast<uint8_t*>(c->v_pool), rows * (int8 ? 1 : 2),
+                  reinterpret_cast<uint8_t*>(int8 ? c->scales : nullptr), sc_bytes, c->err_word, int(kErrBlockId));
+}
+
+int pkv_copy_blocks(const pkv_cache_desc* c, const int32_t* src_ids, const int32_t* dst_ids, int32_t n,
+                    void* stream) {
+    return copy_slabs(c, false, src_ids, dst_ids, n, stream);
+}
+
+int pkv_copy_slots(const pkv_cache_desc* c, const int32_t* src_slots, const int32_t* dst_slots, int32_t n,
+                   void* stream) {
+    return copy_slabs(c, true, src_slots, dst_slots, n, stream);
 }
 
 static int launch_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_lens, int32_t B, int32_t Hq,

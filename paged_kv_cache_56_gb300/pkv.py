@@ -50,6 +50,7 @@ EXPORTED = (
     "pkv_quantize_blocks_from", "pkv_decode_attention", "pkv_splitk_reduce",
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
     "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step", "pkv_decode_layers",
+    "pkv_fork", "pkv_cow_block", "pkv_block_refs", "pkv_copy_blocks", "pkv_copy_slots",
 )
 
 
@@ -93,6 +94,11 @@ def lib() -> ctypes.CDLL:
             "pkv_append_block": (ctypes.c_int, [_VP, _I64, _I32P]),
             "pkv_free": (ctypes.c_int, [_VP, _I64]),
             "pkv_attach_shared": (ctypes.c_int, [_VP, _I64, _I32P, _I32]),
+            "pkv_fork": (ctypes.c_int, [_VP, _I64, _I64]),
+            "pkv_cow_block": (ctypes.c_int, [_VP, _I64, _I32, _I32P, _I32P]),
+            "pkv_block_refs": (ctypes.c_int, [_VP, _I32]),
+            "pkv_copy_blocks": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP]),
+            "pkv_copy_slots": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP]),
             "pkv_num_free": (ctypes.c_int, [_VP]),
             "pkv_request_table": (ctypes.c_int, [_VP, _I64, _I32P, _I32]),
             "pkv_free_list": (ctypes.c_int, [_VP, _I32P, _I32]),
@@ -194,6 +200,24 @@ def pkv_free(h, req_id: int) -> None:
     _check("pkv_free", lib().pkv_free(h, req_id))
 
 
+def pkv_fork(h, parent: int, child: int) -> None:
+    _check("pkv_fork", lib().pkv_fork(h, parent, child))
+
+
+def pkv_cow_block(h, req_id: int, index: int):
+    """(old, new) block ids if a private copy replaced a shared block, else None."""
+    src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    _check("pkv_cow_block", lib().pkv_cow_block(h, req_id, index, ctypes.byref(src), ctypes.byref(dst)))
+    return None if src.value < 0 else (src.value, dst.value)
+
+
+def pkv_block_refs(h, block: int) -> int:
+    rc = lib().pkv_block_refs(h, block)
+    if rc < 0:
+        raise PkvError("pkv_block_refs", rc)
+    return rc
+
+
 def pkv_attach_shared(h, req_id: int, ids) -> None:
     a = _host_i32(ids)
     _check("pkv_attach_shared", lib().pkv_attach_shared(h, req_id, a.ctypes.data_as(_I32P), a.size))
@@ -262,6 +286,20 @@ def pkv_quantize_full_blocks(desc: CacheDesc, block_ids: torch.Tensor, slots: to
     sp = _dev(slots, "slots", torch.int32, M)
     _check("pkv_quantize_full_blocks",
            lib().pkv_quantize_full_blocks(_desc_ptr(desc), bp, sp, M, _stream(stream)))
+
+
+def pkv_copy_blocks(desc: CacheDesc, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=None) -> None:
+    n = src_ids.numel()
+    sp = _dev(src_ids, "src_ids", torch.int32, n)
+    dp = _dev(dst_ids, "dst_ids", torch.int32, n)
+    _check("pkv_copy_blocks", lib().pkv_copy_blocks(_desc_ptr(desc), sp, dp, n, _stream(stream)))
+
+
+def pkv_copy_slots(desc: CacheDesc, src_slots: torch.Tensor, dst_slots: torch.Tensor, stream=None) -> None:
+    n = src_slots.numel()
+    sp = _dev(src_slots, "src_slots", torch.int32, n)
+    dp = _dev(dst_slots, "dst_slots", torch.int32, n)
+    _check("pkv_copy_slots", lib().pkv_copy_slots(_desc_ptr(desc), sp, dp, n, _stream(stream)))
 
 
 def pkv_quantize_blocks_from(desc: CacheDesc, k_src: torch.Tensor, v_src: torch.Tensor,

@@ -110,6 +110,7 @@ class StepPlan:
     fill_blocks: np.ndarray    # [B] block that filled this step, or -1
     tables: np.ndarray         # [B, max_blocks]
     tables_changed: bool = True
+    cow: list = None           # (old, new) block pairs to copy before the step's writes
 
 
 class PagedKVCache:
@@ -121,15 +122,23 @@ class PagedKVCache:
         self.L = num_layers
         self.bs = block_size
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
-        self.int8 = int8
+        # int8: one flag for every layer, or one per layer -- mixed precision
+        # ("轻量级推理引擎实战" §3.2: bf16 for the sensitive first and last
+        # layers, INT8 in between); each layer's descriptor carries its dtype
+        flags = [bool(int8)] * num_layers if isinstance(int8, (bool, int)) else [bool(x) for x in int8]
+        if len(flags) != num_layers:
+            raise ValueError("int8 needs one flag per layer")
+        self.layer_int8 = flags
+        self.int8 = any(flags)  # some layer keeps INT8 blocks: fills are tracked
         self.max_slots = max_slots
         self.max_blocks = max_blocks_per_seq
         self.device = device
-        self.layers = [LayerCache(num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, int8,
-                                  max_slots, device) for _ in range(num_layers)]
+        self.layers = [LayerCache(num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, f,
+                                  max_slots, device) for f in flags]
         self.alloc = pkv.pkv_allocator_create(num_blocks, block_size, initial_order)
         self.free_slots = list(range(max_slots))
         self.seqs: dict[int, Seq] = {}
+        self.forked = False  # set by fork(): only then can a block have several holders
 
     def close(self):
         if self.alloc is not None:
@@ -153,6 +162,28 @@ class PagedKVCache:
         self.seqs[req_id] = s
         return s
 
+    def fork(self, parent: int, child: int, stream=None) -> Seq:
+        """Copy-on-write fork ("vLLM核心概念" §3.2: parallel sampling, beam
+        search): the child holds every block of the parent and continues from
+        the same length; blocks are copied only when a holder writes into a
+        shared one (plan_step). INT8: the partly filled block lives in the
+        slot's bf16 tail, which is copied to the child's slot here."""
+        if not self.free_slots:
+            raise RuntimeError("no free sequence slot")
+        p = self.seqs[parent]
+        pkv.pkv_fork(self.alloc, parent, child)
+        self.forked = True
+        s = Seq(child, self.free_slots.pop(0), p.length)
+        self.seqs[child] = s
+        if self.int8 and p.length % self.bs:
+            dev = self.layers[0].k_pool.device
+            src = torch.tensor([p.slot], dtype=torch.int32, device=dev)
+            dst = torch.tensor([s.slot], dtype=torch.int32, device=dev)
+            for lc in self.layers:
+                if lc.int8:
+                    pkv.pkv_copy_slots(lc.desc, src, dst, stream)
+        return s
+
     def remove_sequence(self, req_id: int) -> None:
         s = self.seqs.pop(req_id)
         pkv.pkv_free(self.alloc, req_id)
@@ -172,12 +203,20 @@ class PagedKVCache:
         fill = np.full(B, -1, np.int32)
         slots = np.empty(B, np.int32)
         changed = False
+        cow = []
         for i, r in enumerate(req_ids):
             s = self.seqs[r]
             p = s.length
             if p % self.bs == 0 and len(self.table(r)) <= p // self.bs:
                 pkv.pkv_append_block(self.alloc, r)
                 changed = True
+            elif self.forked and p % self.bs:
+                # the row goes into a partly filled block: if a fork left it
+                # shared, this request takes a private copy first
+                pair = pkv.pkv_cow_block(self.alloc, r, p // self.bs)
+                if pair is not None:
+                    cow.append(pair)
+                    changed = True
             pos[i] = p
             slots[i] = s.slot
         tables = pkv.pkv_build_block_tables(self.alloc, req_ids, self.max_blocks, tables_out)
@@ -187,7 +226,21 @@ class PagedKVCache:
             if self.int8 and (p + 1) % self.bs == 0:
                 fill[i] = blk[i]
         return StepPlan(positions=pos, ctx_lens=pos + 1, offsets=pos % self.bs, block_ids=blk,
-                        slots=slots, fill_blocks=fill, tables=tables, tables_changed=changed)
+                        slots=slots, fill_blocks=fill, tables=tables, tables_changed=changed, cow=cow)
+
+    def apply_cow(self, plan: StepPlan, stream=None) -> None:
+        """Device half of the plan's copy-on-write: the old blocks' rows into
+        the new ones, every layer, before the step writes. An INT8 block that
+        has not filled holds no pool data (its rows are in the slot's tail), so
+        there is nothing to copy."""
+        if not plan.cow or all(self.layer_int8):
+            return
+        dev = self.layers[0].k_pool.device
+        src = torch.tensor([a for a, _ in plan.cow], dtype=torch.int32, device=dev)
+        dst = torch.tensor([b for _, b in plan.cow], dtype=torch.int32, device=dev)
+        for lc in self.layers:
+            if not lc.int8:
+                pkv.pkv_copy_blocks(lc.desc, src, dst, stream)
 
     def commit_step(self, req_ids) -> None:
         for r in req_ids:
@@ -213,7 +266,7 @@ def prefill(cache: PagedKVCache, layer: int, req_ids, k_rows, v_rows, starts=Non
     dev = lc.k_pool.device
     starts = [0] * len(req_ids) if starts is None else list(starts)
     tabs = [cache.table(r) for r in req_ids]
-    if not cache.int8:
+    if not lc.int8:
         blk, off = [], []
         for t, s0, k in zip(tabs, starts, k_rows):
             pos = np.arange(s0, s0 + k.shape[0])
@@ -317,7 +370,7 @@ def run_layers(cache: PagedKVCache, bufs: StepBuffers, q, k_new, v_new, out, sm_
     B = bufs.B
     for li, lc in enumerate(cache.layers):
         pkv.pkv_append_kv(lc.desc, k_new[li], v_new[li], bufs.blk[:B], bufs.off[:B], bufs.slot[:B], stream)
-        if cache.int8 and (quantize == "always" or (plan is not None and (plan.fill_blocks >= 0).any())):
+        if lc.int8 and (quantize == "always" or (plan is not None and (plan.fill_blocks >= 0).any())):
             pkv.pkv_quantize_full_blocks(lc.desc, bufs.fill[:B], bufs.slot[:B], stream)
         pkv.pkv_decode_attention(lc.desc, q[li], bufs.tab[:B], bufs.ctx[:B], bufs.slot[:B], sm_scale, out[li],
                                  bufs.split_tokens, bufs.max_splits, bufs.ws_o, bufs.ws_ml, bufs.ws_count, stream)
@@ -327,6 +380,7 @@ def decode_step(cache: PagedKVCache, bufs: StepBuffers, req_ids, q, k_new, v_new
                 stream=None) -> StepPlan:
     """Host plan + upload + kernels of one decode step; advances the sequences."""
     plan = cache.plan_step(req_ids)
+    cache.apply_cow(plan, stream)
     bufs.upload(plan)
     run_layers(cache, bufs, q, k_new, v_new, out, sm_scale, "auto", plan, stream)
     cache.commit_step(req_ids)
@@ -364,8 +418,9 @@ class GraphStep:
 
     def launches_per_step(self) -> int:
         per_attn = 2 if (self.bufs.split_tokens and self.bufs.ws_count is None) else 1
-        update = 0 if self.fused else 1 + (1 if self.cache.int8 else 0)
-        return self.cache.L * (update + self.R * per_attn)
+        if self.fused:
+            return self.cache.L * self.R * per_attn
+        return sum(1 + int(f) + self.R * per_attn for f in self.cache.layer_int8)
 
     def _layers(self, attention_only: bool = False) -> None:
         c, b = self.cache, self.bufs
@@ -374,7 +429,7 @@ class GraphStep:
             fused_here = self.fused and not attention_only
             if not attention_only and not self.fused:
                 pkv.pkv_append_kv(lc.desc, self.k[li], self.v[li], b.blk[:B], b.off[:B], b.slot[:B])
-                if c.int8:
+                if lc.int8:
                     pkv.pkv_quantize_full_blocks(lc.desc, b.fill[:B], b.slot[:B])
             for r in range(self.R):
                 qi = li * self.R + r

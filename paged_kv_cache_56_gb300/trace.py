@@ -155,6 +155,7 @@ class TraceDriver:
             return [], None
         rids = self.batch_order()
         plan = c.plan_step(rids)
+        c.apply_cow(plan)
         self.bufs.upload(plan)
         B = len(rids)
         pos = torch.tensor(plan.positions, dtype=torch.int64)
@@ -185,7 +186,7 @@ class TraceDriver:
                                     self.out[li, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
             else:
                 pkv.pkv_append_kv(lc.desc, k, v, b.blk[:B], b.off[:B], b.slot[:B])
-                if c.int8 and (plan.fill_blocks >= 0).any():
+                if lc.int8 and (plan.fill_blocks >= 0).any():
                     pkv.pkv_quantize_full_blocks(lc.desc, b.fill[:B], b.slot[:B])
                 pkv.pkv_decode_attention(lc.desc, q, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
                                          self.out[li, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml,

@@ -37,7 +37,7 @@ class Workload:
     """L layers, B sequences with prior lengths ``prior``; decode steps t = 0, 1, ..."""
 
     def __init__(self, seed: int, num_layers: int, prior, Hq: int, Hkv: int, d: int, bs: int,
-                 num_blocks: int, int8: bool, split_tokens: int = 0, max_blocks: int | None = None,
+                 num_blocks: int, int8, split_tokens: int = 0, max_blocks: int | None = None,
                  head_scale: bool = False, outliers: bool = False, shuffle: bool = True,
                  req_ids=None, device="cuda", fused_merge: bool = True, graph: bool = False, repeat: int = 1,
                  fused_step: bool | None = None):
@@ -121,6 +121,7 @@ class Workload:
             self.step_no += 1
             return out
         plan = self.cache.plan_step(self.req_ids)
+        self.cache.apply_cow(plan)
         self.bufs.upload(plan)
         first = self.gs is None
         if first:
@@ -144,7 +145,7 @@ class Workload:
     # -- oracle ---------------------------------------------------------------
     def history(self, layer: int, i: int, n: int) -> SequenceHistory:
         r = self.req_ids[i]
-        h = SequenceHistory(self.Hkv, self.d, self.bs, self.int8)
+        h = SequenceHistory(self.Hkv, self.d, self.bs, self.cache.layer_int8[layer])
         pos = torch.arange(n)
         h.append(self.kv(layer, synth.KIND_K, r, pos, "cpu").float().numpy(),
                  self.kv(layer, synth.KIND_V, r, pos, "cpu").float().numpy())
@@ -177,11 +178,12 @@ class Workload:
         history byte for byte; returns the number of blocks compared."""
         h = self.history(layer, i, n)
         lc = self.cache.layers[layer]
+        int8 = lc.int8
         tab = self.cache.table(self.req_ids[i])
         nf = n // self.bs
         nb = -(-n // self.bs)
-        ids = torch.tensor(tab[: (nf if self.int8 else nb)], dtype=torch.long, device=lc.k_pool.device)
-        if self.int8:
+        ids = torch.tensor(tab[: (nf if int8 else nb)], dtype=torch.long, device=lc.k_pool.device)
+        if int8:
             kp = lc.k_pool[ids].cpu().numpy()
             vp = lc.v_pool[ids].cpu().numpy()
             sc = lc.scales[ids].cpu().numpy()

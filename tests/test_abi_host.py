@@ -84,6 +84,11 @@ def test_argument_validation(L):
     assert L.pkv_append_kv(ctypes.byref(d), 16, 16, 16, 16, 16, 0, None) == pkv.PKV_OK  # T = 0
     assert L.pkv_append_kv(ctypes.byref(d), 16, 16, None, 16, 16, 3, None) == pkv.PKV_ERR_INVALID
     assert L.pkv_quantize_full_blocks(ctypes.byref(d), 16, 16, 1, None) == pkv.PKV_ERR_INVALID  # BF16 cache
+    assert L.pkv_copy_blocks(ctypes.byref(d), 16, 16, 0, None) == pkv.PKV_OK  # n = 0
+    assert L.pkv_copy_blocks(ctypes.byref(d), 16, 16, -1, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_copy_blocks(ctypes.byref(d), None, 16, 2, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_copy_blocks(None, 16, 16, 2, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_copy_slots(ctypes.byref(d), 16, 16, 2, None) == pkv.PKV_ERR_INVALID  # BF16 cache: no tails
     assert L.pkv_splitk_reduce(16, 16, 16, 1, 4, 96, 16, 2, 16, None) == pkv.PKV_ERR_UNSUPPORTED
     assert L.pkv_splitk_reduce(16, 16, 16, 1, 4, 128, 0, 2, 16, None) == pkv.PKV_ERR_INVALID
     assert pkv.pkv_splitk_ws_o_bytes(2, 3, 128, 5) == 2 * 3 * 5 * 128 * 4
@@ -193,5 +198,99 @@ def test_page_sizing_through_the_allocator(L):
     try:
         ids = pkv.pkv_alloc(h, 1, -(-600 // 16))
         assert len(ids) == 38 and pkv.pkv_num_free(h) == 2010
+    finally:
+        pkv.pkv_allocator_destroy(h)
+
+
+def test_forks_and_cow_replay_oracle_ids(L):
+    """Random alloc / append / fork / cow / free through the C ABI and through
+    the oracle pool: identical ids, tables, free lists and reference counts."""
+    rng = random.Random(99)
+    n = 61
+    order = rng.sample(range(n), n)
+    h = pkv.pkv_allocator_create(n, 16, order)
+    ref = FreeBlockPool(n, order)
+    live, nxt = [], 0
+    try:
+        for i in range(20_000):
+            u = rng.random()
+            if u < 0.15 or not live:
+                k = rng.randint(0, 5)
+                try:
+                    want = ref.alloc(nxt, k)
+                except OutOfBlocks:
+                    with pytest.raises(pkv.PkvError) as e:
+                        pkv.pkv_alloc(h, nxt, k)
+                    assert e.value.code == pkv.PKV_ERR_OOM
+                else:
+                    assert pkv.pkv_alloc(h, nxt, k) == want
+                    live.append(nxt)
+                nxt += 1
+            elif u < 0.35:
+                r = rng.choice(live)
+                want = ref.append_block(r)
+                if want is None:
+                    with pytest.raises(pkv.PkvError):
+                        pkv.pkv_append_block(h, r)
+                else:
+                    assert pkv.pkv_append_block(h, r) == want
+            elif u < 0.5:
+                r = rng.choice(live)
+                ref.fork(r, nxt)
+                pkv.pkv_fork(h, r, nxt)
+                live.append(nxt)
+                nxt += 1
+            elif u < 0.8:
+                r = rng.choice(live)
+                t = ref.table(r)
+                if t:
+                    idx = rng.randrange(len(t))
+                    try:
+                        want = ref.cow(r, idx)
+                    except OutOfBlocks:
+                        with pytest.raises(pkv.PkvError) as e:
+                            pkv.pkv_cow_block(h, r, idx)
+                        assert e.value.code == pkv.PKV_ERR_OOM
+                    else:
+                        assert pkv.pkv_cow_block(h, r, idx) == want
+            else:
+                r = live.pop(rng.randrange(len(live)))
+                ref.free(r)
+                pkv.pkv_free(h, r)
+            if i % 499 == 0:
+                assert pkv.pkv_free_list(h) == ref.free_list
+                for r in live[:6]:
+                    t = pkv.pkv_request_table(h, r)
+                    assert t == ref.table(r)
+                    assert [pkv.pkv_block_refs(h, b) for b in t] == [ref.refs(b) for b in t]
+        assert pkv.pkv_free_list(h) == ref.free_list
+        for b in range(n):
+            assert pkv.pkv_block_refs(h, b) == ref.refs(b)
+    finally:
+        pkv.pkv_allocator_destroy(h)
+
+
+def test_fork_and_cow_errors(L):
+    h = pkv.pkv_allocator_create(6, 16)
+    try:
+        prefix = pkv.pkv_alloc(h, -1, 1)
+        pkv.pkv_alloc(h, 1, 1)
+        pkv.pkv_attach_shared(h, 1, prefix)
+        for fn, args, code in [(pkv.pkv_fork, (9, 2), pkv.PKV_ERR_NOT_FOUND),
+                               (pkv.pkv_fork, (1, -1), pkv.PKV_ERR_EXISTS),
+                               (pkv.pkv_cow_block, (1, 0), pkv.PKV_ERR_INVALID),   # pinned prefix
+                               (pkv.pkv_cow_block, (1, 2), pkv.PKV_ERR_INVALID),   # past the table
+                               (pkv.pkv_cow_block, (9, 0), pkv.PKV_ERR_NOT_FOUND),
+                               (pkv.pkv_block_refs, (6,), pkv.PKV_ERR_INVALID)]:
+            with pytest.raises(pkv.PkvError) as e:
+                fn(h, *args)
+            assert e.value.code == code, (fn, args)
+        pkv.pkv_fork(h, 1, 2)
+        assert pkv.pkv_request_table(h, 2) == prefix + [1]
+        assert pkv.pkv_block_refs(h, 1) == 2 and pkv.pkv_block_refs(h, prefix[0]) == 1
+        assert pkv.pkv_cow_block(h, 2, 1) == (1, 2)
+        assert pkv.pkv_cow_block(h, 1, 1) is None
+        pkv.pkv_free(h, 1)
+        assert pkv.pkv_free_list(h) == [3, 4, 5, 1]
     finally:
         pkv.pkv_allocator_destroy(h)

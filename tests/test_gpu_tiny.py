@@ -172,3 +172,24 @@ def test_single_kv_head_odd_pool(split):
     assert w.error_bits() == 0
     for i in range(w.B):
         w.check_pool_bytes(0, i, w.prior[i] + 20)
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_mixed_precision_layers(graph):
+    """Per-layer cache precision ("轻量级推理引擎实战" §3.2: bf16 for the first
+    and last layers, INT8 in between) through one step path: every layer
+    against the oracle in its own precision, pools byte for byte."""
+    flags = (False, True, True, False)
+    w = Workload(seed=41, num_layers=4, prior=(15, 16, 47, 1), Hq=4, Hkv=2, d=64, bs=16, num_blocks=96,
+                 int8=flags, split_tokens=32, max_blocks=9, graph=graph)
+    assert [lc.int8 for lc in w.cache.layers] == list(flags)
+    for t in range(18):
+        out = w.step().float().cpu().numpy()
+        if t % 6 == 5 or t == 0:
+            for layer in range(4):
+                for i in range(w.B):
+                    assert_close(out[layer, i], w.oracle_out(layer, i, t), f"step {t} layer {layer} seq {i}")
+    assert w.error_bits() == 0
+    for layer in range(4):
+        for i in range(w.B):
+            w.check_pool_bytes(layer, i, w.prior[i] + 18)
