@@ -60,6 +60,7 @@ extern "C" {
 #define PKV_DEVERR_CTX_LEN     4  /* context length < 0 or > max_blocks * block_size */
 #define PKV_DEVERR_OFFSET      8  /* in-block offset < 0 or >= block_size */
 #define PKV_DEVERR_TIMEOUT    16  /* a bounded wait on an asynchronous copy expired */
+#define PKV_DEVERR_SEGMENT    32  /* a work-list entry out of range (pkv_decode_layers_planned) */
 
 #define PKV_DTYPE_BF16 0
 #define PKV_DTYPE_INT8 1
@@ -290,6 +291,44 @@ int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const voi
                       const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
                       const int32_t* slots, int32_t B, float sm_scale, int32_t split_tokens,
                       int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count, void* stream);
+
+/* Work list for decode over sequences of very different lengths (a
+ * continuous-batching step): pkv_plan_segments (host) lays the (sequence,
+ * kv head) token runs of the step end to end, each rounded up to `granule`
+ * tokens (a multiple of 16 and of block_size), and cuts them into num_ctas
+ * pieces of equal length -- one wave of CTAs that start and finish
+ * together. A piece is a list of units {b, t0, t1, kvh | j << 8 | ns << 20}:
+ * tokens [t0, t1) of kv head kvh of sequence b, split j of the ns splits of
+ * that pair (a sequence with ctx 0 gets one empty unit: its zero row).
+ * Outputs: seg_offsets[num_ctas + 1] (piece c = units seg_offsets[c] ..
+ * seg_offsets[c+1]-1), segs[seg_cap][4], info[4] = {units, most splits of one
+ * pair, longest unit in tokens, pieces used}. PKV_ERR_TOO_LARGE when seg_cap
+ * units do not suffice (or a pair would need more than 4095 splits);
+ * PKV_ERR_INVALID for bad arguments (num_kv_heads must be < 256). Host memory
+ * only; the caller copies seg_offsets and segs to the device. */
+int pkv_plan_segments(const int32_t* ctx_lens, int32_t B, int32_t num_kv_heads, int32_t granule,
+                      int32_t num_ctas, int32_t* seg_offsets, int32_t* segs, int32_t seg_cap, int32_t* info);
+
+typedef struct pkv_segment_plan {
+    const int32_t* seg_offsets;  /* device int32 [num_ctas + 1] */
+    const int32_t* segs;         /* device int32 [units][4], 16-byte aligned */
+    int32_t num_ctas;            /* CTAs to launch (pieces; unused pieces are empty) */
+    int32_t max_splits;          /* >= the most splits of one pair, <= 4095: the workspace's split extent */
+    int32_t max_unit_tokens;     /* >= the longest unit */
+} pkv_segment_plan;
+
+/* pkv_decode_layers over a work list instead of a uniform split: each of
+ * plan->num_ctas CTAs runs its units back to back; the partial states of a
+ * pair cut into several units are merged in the same kernel by the last one
+ * to arrive (ws_count is required, zero before the first call and left at
+ * zero; the workspace is sized for plan->max_splits). Same results as
+ * pkv_decode_layers up to the order of the fp32 softmax merge. */
+int pkv_decode_layers_planned(const pkv_cache_desc* descs, int32_t num_layers, const void* q,
+                              int64_t q_layer_stride, const void* k_new, const void* v_new,
+                              int64_t kv_layer_stride, void* out, int64_t out_layer_stride,
+                              const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                              const int32_t* slots, int32_t B, float sm_scale, const pkv_segment_plan* plan,
+                              float* ws_o, float* ws_ml, int32_t* ws_count, void* stream);
 
 /* CTAs of the decode kernel for this cache shape that fit on one SM at once
  * (registers and shared memory), for a given split_tokens (0 = none) and

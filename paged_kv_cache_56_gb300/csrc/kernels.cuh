@@ -47,6 +47,7 @@ constexpr int kErrSlot = 2;
 constexpr int kErrCtxLen = 4;
 constexpr int kErrOffset = 8;
 constexpr int kErrTimeout = 16;
+constexpr int kErrSegment = 32;
 
 __device__ __forceinline__ void report(int32_t* err, int bits) {
     if (err) atomicOr(err, bits);
@@ -71,6 +72,9 @@ struct DecodeParams {
     int32_t* err;
     int32_t Hq, Hkv, bs, max_blocks, num_blocks, max_slots, split_tokens, max_splits;
     int32_t tab_cap;  // block-table entries the shared table holds (even)
+    const int32_t* seg_offsets;  // work list (decode_segments_kernel): [gridDim.x + 1]
+    const int32_t* segs;         // [n][4]
+    int32_t B;
     float qscale;     // sm_scale * log2(e)
 };
 
@@ -278,8 +282,18 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
     const float p2 = fast_exp2(s[2] - st.m[0]), p3 = fast_exp2(s[3] - st.m[1]);
     st.l[0] += p0 + p2;
     st.l[1] += p1 + p3;
-    const uint32_t b0 = movmatrix_t(pack2<F16>(p0 * vsc, p1 * vsc));
-    const uint32_t b1 = movmatrix_t(pack2<F16>(p2 * vsc, p3 * vsc));
+    const float x0 = p0 * vsc, x1 = p1 * vsc, x2 = p2 * vsc, x3 = p3 * vsc;
+    const uint32_t w01 = pack2<F16>(x0, x1), w23 = pack2<F16>(x2, x3);
+    const uint32_t b0 = movmatrix_t(w01), b1 = movmatrix_t(w23);
+    // bf16 keeps 8 bits of a weight (a relative error up to 2^-9, visible when
+    // a few tokens dominate); the rounding residual goes in as a second bf16
+    // term, so that P enters the sum to ~2^-17 like the fp32 l beside it
+    uint32_t b0l = 0u, b1l = 0u;
+    if (!F16) {
+        const float2 h01 = bf16x2_to_f2(w01), h23 = bf16x2_to_f2(w23);
+        b0l = movmatrix_t(pack2<false>(x0 - h01.x, x1 - h01.y));
+        b1l = movmatrix_t(pack2<false>(x2 - h23.x, x3 - h23.y));
+    }
     // ---- O^T += V^T . P^T
     uint32_t v0[Gm::kVW], v1[Gm::kVW], v2[Gm::kVW], v3[Gm::kVW];
     load_run<Gm::kVB>(V, 2 * t, g * Gm::kVB, v0);
@@ -310,6 +324,7 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
             const uint32_t a0 = __byte_perm(v0[j], v1[j], 0x5410), a1 = __byte_perm(v0[j], v1[j], 0x7632);
             const uint32_t a2 = __byte_perm(v2[j], v3[j], 0x5410), a3 = __byte_perm(v2[j], v3[j], 0x7632);
             mma16816<false>(st.acc[j], a0, a1, a2, a3, b0, b1);
+            mma16816<false>(st.acc[j], a0, a1, a2, a3, b0l, b1l);
         }
     }
 }
@@ -431,13 +446,21 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int D, int G, bool INT8, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
+// One unit of decode work: kv head kvh of sequence b over tokens [t0, t1) --
+// split j of ns (SEG: the unit's own range and count; else split blockIdx.x of
+// the context cut every split_tokens). kb: tiles this warp has consumed in
+// earlier units of the CTA (ring stage and mbarrier phase continue from it);
+// init: the mbarriers still need initialising. Returns the updated count, or
+// its complement (negative) when the unit ended before initialising them.
+template <int D, int G, bool INT8, bool SPLIT, bool SEG>
+__device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem, const int b, const int kvh,
+                                            const int j, const int seg_t0, const int seg_t1, const int seg_ns,
+                                            const bool init, const int kb) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
+    static_assert(SPLIT || !SEG, "work-list units are splits");
     using T = DecodeTraits<D, INT8>;
     using Gm = Geom<D, INT8>;
     constexpr int STAGES = T::kStages;
-    extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
     int32_t* tab = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
@@ -448,10 +471,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     auto mo_of = [&](int w) { return reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes); };
     auto mml_of = [&](int w) { return mo_of(w) + G * D; };
 
-    const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    pdl_launch_dependents();
+    const int kb0 = SEG ? kb : 0;
 
     // Before pdl_wait() this kernel reads only what no preceding kernel of the
     // step writes: context lengths, block tables, slots, and the blocks (and
@@ -462,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         if (tid == 0 && j == 0) report(p.err, kErrCtxLen);
         ctx = 0;
     }
-    const int t0 = SPLIT ? j * p.split_tokens : 0;
-    const int t1 = SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
-    if (t0 >= t1 && j > 0) return;  // this split lies past the context
+    const int t0 = SEG ? seg_t0 : SPLIT ? j * p.split_tokens : 0;
+    const int t1 = SEG ? min(ctx, seg_t1) : SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
+    if (t0 >= t1 && (SEG ? ctx > 0 : j > 0)) return init ? ~kb0 : kb0;  // past the context
 
     const int nfull = INT8 ? (ctx / p.bs) * p.bs : ctx;
     const int pool_end = min(t1, nfull);
@@ -479,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     const uint32_t bar0 = smem_addr(bars);
     const uint32_t stage0 = smem_addr(stages);
     auto bar_of = [&](int s) { return bar0 + uint32_t(warp * STAGES + s) * 8u; };
+    // this warp's i-th tile of the unit uses ring stage (kb + i) % STAGES, and
+    // waits for completion number (kb + i) / STAGES of that stage's mbarrier
     auto stage_of = [&](int s) { return stage0 + uint32_t(warp * STAGES + s) * T::kStageBytes; };
 
-    if (lane == 0)
+    if ((!SEG || init) && lane == 0)
         for (int s = 0; s < STAGES; ++s) mbar_init(bar_of(s), 1);
     const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks + blk0;
     for (int i = tid; i < nblk; i += kThreads) {
@@ -524,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     if (lane == 0)
         for (int s = 0; s < STAGES; ++s) {
             const int tile = warp + s * kWarps;
-            if (tile < nt_stable) issue(tile, s);
+            if (tile < nt_stable) issue(tile, (kb0 + s) % STAGES);
         }
     if (INT8) load_scales(0, nblk_stable);
 
@@ -581,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     if (lane == 0)
         for (int s = 0; s < STAGES; ++s) {
             const int tile = warp + s * kWarps;
-            if (tile >= nt_stable && tile < nt) issue(tile, s);
+            if (tile >= nt_stable && tile < nt) issue(tile, (kb0 + s) % STAGES);
         }
     if (INT8) load_scales(nblk_stable, nblk);
 
@@ -633,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     int k = 0;
     bool timed_out = false;
     for (int tile = warp; tile < nt; tile += kWarps, ++k) {
-        const int s = k % STAGES;
-        if (!wait_phase(bar_of(s), uint32_t(k / STAGES) & 1u)) {
+        const int s = (kb0 + k) % STAGES;
+        if (!wait_phase(bar_of(s), uint32_t((kb0 + k) / STAGES) & 1u)) {
             timed_out = true;
             break;
         }
@@ -662,8 +686,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         // so that no copy lands in shared memory after the CTA has exited.
         if (lane == 0) report(p.err, kErrTimeout);
         for (int kk = k; kk < k + STAGES && warp + kk * kWarps < nt; ++kk)
-            (void)wait_phase(bar_of(kk % STAGES), uint32_t(kk / STAGES) & 1u);
+            (void)wait_phase(bar_of((kb0 + kk) % STAGES), uint32_t((kb0 + kk) / STAGES) & 1u);
     }
+    const int kbn = kb0 + k;
 
     // ---- merge: lanes of a warp hold disjoint dims; sum l over the 8 g lanes
 #pragma unroll
@@ -694,11 +719,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         // no tokens: a zero row (no partials, no counter)
         for (int e = tid; e < G * D; e += kThreads)
             reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G) * D + e] = __float2bfloat16_rn(0.f);
-        return;
+        return kbn;
     }
     // With the fused merge, a sequence whose context fits one split has
     // nothing to merge: its only split writes the output itself.
-    const int ns = SPLIT ? (ctx + p.split_tokens - 1) / p.split_tokens : 1;
+    const int ns = SEG ? seg_ns : SPLIT ? (ctx + p.split_tokens - 1) / p.split_tokens : 1;
     const bool partial = SPLIT && !(p.ws_count && ns == 1);
     for (int e = tid; e < G * D; e += kThreads) {
         const int h = e / D, dim = e % D;
@@ -733,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         __syncthreads();
         if (tid == 0) s_last = atom_add_acq_rel_gpu(cnt, 1) == ns - 1;
         __syncthreads();
-        if (!s_last) return;
+        if (!s_last) return kbn;
         constexpr int EPT = (G * D + kThreads - 1) / kThreads;  // output elements per thread
         constexpr int QB = EPT >= 48 ? 1 : 48 / EPT;   // splits per batch of loads
         float* wsm = reinterpret_cast<float*>(stages);  // [G][ns] weights, then [G] sums
@@ -813,6 +838,46 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
             }
         }
         if (tid == 0) *cnt = 0;  // ready for the next call
+    }
+    return kbn;
+}
+
+// Grid (split, kv head, sequence): one unit per CTA.
+template <int D, int G, bool INT8, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
+    (void)decode_unit<D, G, INT8, SPLIT, false>(p, smem, blockIdx.z, blockIdx.y, blockIdx.x, 0, 0, 0, true, 0);
+}
+
+// Work list: CTA c runs units seg_offsets[c] .. seg_offsets[c+1]-1 of segs,
+// each {b, t0, t1, kvh | j << 8 | ns << 20} -- a balanced cut of all the
+// step's (sequence, kv head) token ranges, one wave of CTAs (see
+// pkv_plan_segments). Units of one CTA run back to back through the same
+// ring; an out-of-range entry is skipped and reported.
+template <int D, int G, bool INT8>
+__global__ void __launch_bounds__(kThreads, kMinCtas) decode_segments_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
+    int kb = 0;
+    const int lo = p.seg_offsets[blockIdx.x], hi = p.seg_offsets[blockIdx.x + 1];
+    bool init = true;
+    for (int i = lo; i < hi; ++i) {
+        const int4 sg = __ldg(reinterpret_cast<const int4*>(p.segs) + i);
+        const int b = sg.x, kvh = sg.w & 0xFF, j = (sg.w >> 8) & 0xFFF, ns = (sg.w >> 20) & 0xFFF;
+        if (b < 0 || b >= p.B || kvh >= p.Hkv || j >= ns || ns > p.max_splits || sg.y < 0 || sg.y > sg.z ||
+            (sg.y % kTile) != 0) {
+            if (threadIdx.x == 0) report(p.err, kErrSegment);
+            continue;
+        }
+        const int r = decode_unit<D, G, INT8, true, true>(p, smem, b, kvh, j, sg.y, sg.z, ns, init, kb);
+        if (r < 0) {
+            kb = ~r;
+        } else {
+            kb = r;
+            init = false;
+        }
+        __syncthreads();  // the next unit reuses the table, ring and merge space
     }
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <utility>
@@ -203,6 +204,25 @@ static DecodeFn pick_g(int g) {
     }
 }
 
+template <int D, bool INT8>
+static DecodeFn pick_seg_g(int g) {
+    switch (g) {
+        case 1: return decode_segments_kernel<D, 1, INT8>;
+        case 2: return decode_segments_kernel<D, 2, INT8>;
+        case 4: return decode_segments_kernel<D, 4, INT8>;
+        case 8: return decode_segments_kernel<D, 8, INT8>;
+        default: return nullptr;
+    }
+}
+
+// The work-list decode instantiation for a shape (state indices 32..47).
+static DecodeFn pick_segments(int d, int g, bool int8, int* index) {
+    const int lg = g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3;
+    *index = 32 + ((d == 128) * 4 + lg) * 2 + int8;
+    if (d == 128) return int8 ? pick_seg_g<128, true>(g) : pick_seg_g<128, false>(g);
+    return int8 ? pick_seg_g<64, true>(g) : pick_seg_g<64, false>(g);
+}
+
 // The decode instantiation for a shape, and a small index for per-kernel state.
 static DecodeFn pick_decode(int d, int g, bool int8, bool split, int* index) {
     const int lg = g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3;
@@ -218,7 +238,7 @@ static DecodeFn pick_decode(int d, int g, bool int8, bool split, int* index) {
 // Raises the kernel's dynamic shared-memory limit (once per kernel, device
 // and size) so that it can be launched or sized with `smem` bytes.
 static int allow_smem(DecodeFn fn, int index, size_t smem) {
-    static int configured[32][64] = {};
+    static int configured[48][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (int(smem) > configured[index][dev]) {
@@ -406,7 +426,7 @@ int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_
 static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
                        const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                        int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml,
-                       int32_t* ws_count, void* out, void* stream) {
+                       int32_t* ws_count, void* out, void* stream, const pkv_segment_plan* plan = nullptr) {
     int st = check_desc(c);
     if (st != PKV_OK) return st;
     if (B < 0 || max_blocks <= 0 || split_tokens < 0 || !(sm_scale == sm_scale)) return PKV_ERR_INVALID;
@@ -417,15 +437,27 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     if (int8 && !slots) return PKV_ERR_INVALID;
     const int64_t max_ctx = int64_t(max_blocks) * c->block_size;
     if (max_ctx > 0x7FFFFFFF) return PKV_ERR_INVALID;
-    const bool split = split_tokens > 0;
-    if (split) {
+    if (plan) {  // work-list mode: the plan replaces the uniform split
+        if (!plan->seg_offsets || !plan->segs || !aligned16(plan->segs) || plan->num_ctas <= 0 ||
+            plan->max_splits <= 0 || plan->max_splits > 4095 || plan->max_unit_tokens < 0 || !ws_count)
+            return PKV_ERR_INVALID;
+        split_tokens = 0;
+        max_splits = plan->max_splits;
+        if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
+    }
+    const bool split = split_tokens > 0 || plan;
+    if (split && !plan) {
         if (split_tokens % c->block_size || split_tokens % kTile) return PKV_ERR_INVALID;
         if (int64_t(max_splits) * split_tokens < max_ctx || max_splits > 65535) return PKV_ERR_INVALID;
         if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
     }
     if (split && ws_count && (reinterpret_cast<uintptr_t>(ws_count) & 3u)) return PKV_ERR_INVALID;
     const int g = c->num_q_heads / c->num_kv_heads;
-    const int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
+    int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
+    if (plan) {
+        tab_cap = std::min<int64_t>(max_blocks, int64_t(plan->max_unit_tokens) / c->block_size + 2);
+        tab_cap += tab_cap & 1;
+    }
     const size_t smem = decode_smem(c->head_dim, int8, tab_cap);
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
@@ -457,11 +489,15 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     p.max_splits = split ? max_splits : 1;
     p.tab_cap = tab_cap;
     p.qscale = sm_scale * 1.4426950408889634f;
+    p.seg_offsets = plan ? plan->seg_offsets : nullptr;
+    p.segs = plan ? plan->segs : nullptr;
+    p.B = B;
 
-    const dim3 grid(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
+    const dim3 grid = plan ? dim3(unsigned(plan->num_ctas), 1u, 1u)
+                           : dim3(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
     auto s = static_cast<cudaStream_t>(stream);
     int index = 0;
-    DecodeFn fn = pick_decode(c->head_dim, g, int8, split, &index);
+    DecodeFn fn = plan ? pick_segments(c->head_dim, g, int8, &index) : pick_decode(c->head_dim, g, int8, split, &index);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
     if ((st = launch(fn, grid, dim3(kThreads), smem, s, p)) != PKV_OK) return st;
@@ -496,6 +532,29 @@ int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const voi
                                    vb ? vb + l * kv_layer_stride : nullptr, block_tables, max_blocks, ctx_lens, slots,
                                    B, sm_scale, split_tokens, max_splits, ws_o, ws_ml, ws_count,
                                    ob + l * out_layer_stride, stream);
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
+}
+
+int pkv_decode_layers_planned(const pkv_cache_desc* descs, int32_t num_layers, const void* q,
+                              int64_t q_layer_stride, const void* k_new, const void* v_new, int64_t kv_layer_stride,
+                              void* out, int64_t out_layer_stride, const int32_t* block_tables, int32_t max_blocks,
+                              const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
+                              const pkv_segment_plan* plan, float* ws_o, float* ws_ml, int32_t* ws_count,
+                              void* stream) {
+    if (!descs || num_layers < 0 || !q || !out || !plan) return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    if ((q_layer_stride | out_layer_stride | (k_new ? kv_layer_stride : 0)) & 15) return PKV_ERR_INVALID;
+    const auto* qb = static_cast<const uint8_t*>(q);
+    const auto* kb = static_cast<const uint8_t*>(k_new);
+    const auto* vb = static_cast<const uint8_t*>(v_new);
+    auto* ob = static_cast<uint8_t*>(out);
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const int rc = decode_impl(descs + l, qb + l * q_layer_stride, kb ? kb + l * kv_layer_stride : nullptr,
+                                   vb ? vb + l * kv_layer_stride : nullptr, block_tables, max_blocks, ctx_lens, slots,
+                                   B, sm_scale, 0, 0, ws_o, ws_ml, ws_count, ob + l * out_layer_stride, stream, plan);
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;

@@ -51,7 +51,7 @@ class TraceDriver:
     def __init__(self, cache: PagedKVCache, seed: int, num_steps: int, max_running: int = 128,
                  prefix_tokens: int = 200, arrival_rate: float = 2.0, prompt_min: int = 16,
                  prompt_max: int = 4096, mean_output: float = 300.0, split_tokens: int = 0,
-                 fused: bool = True):
+                 fused: bool = True, work_list: bool = False):
         self.cache = cache
         self.seed = seed
         self.max_running = max_running
@@ -66,7 +66,15 @@ class TraceDriver:
         self.finished: list[Request] = []
         self.step_no = 0
         self._next_arrival = 0
-        self.bufs = StepBuffers(cache, max_running, split_tokens, fused_merge=True)
+        # work_list: each step's (sequence, kv head) token runs are cut into one
+        # wave of equal pieces (pkv_plan_segments) instead of a uniform split
+        self.work_list = work_list
+        ctas = 0
+        if work_list:
+            sms = torch.cuda.get_device_properties(cache.device).multi_processor_count
+            ctas = sms * pkv.pkv_decode_ctas_per_sm(cache.layers[0].desc, max(split_tokens, cache.bs),
+                                                    cache.max_blocks)
+        self.bufs = StepBuffers(cache, max_running, split_tokens, fused_merge=True, work_list_ctas=ctas)
         self.out = torch.empty((cache.L, max_running, cache.hq, cache.d), dtype=torch.bfloat16,
                                device=cache.device)
         self.prefix_ids = []
@@ -168,8 +176,13 @@ class TraceDriver:
             vs = torch.stack([x[2] for x in inputs])
             if events is not None:
                 events[0].record()
-            pkv.pkv_decode_layers(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
-                                  self.out[:, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
+            if self.work_list:
+                pkv.pkv_decode_layers_planned(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B],
+                                              self.sm_scale, self.out[:, :B], b.seg_plan, b.ws_o, b.ws_ml,
+                                              b.ws_count)
+            else:
+                pkv.pkv_decode_layers(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
+                                      self.out[:, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
             if events is not None:
                 events[1].record()
             c.commit_step(rids)
