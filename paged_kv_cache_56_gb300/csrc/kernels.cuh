@@ -446,16 +446,74 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
     }
 }
 
+// The step update of (sequence b, kv head kvh) whose context now ends at
+// token ctx-1: writes that token's K/V row (k_new / v_new) into the cache --
+// the slot's bf16 tail (INT8) or pool block `id` (bf16) -- and, in INT8 mode,
+// quantizes block `id` if the row filled it ("轻量级推理引擎实战" §3,
+// quantize-on-fill). Called by every thread of the CTA; ends with a barrier.
+template <int D, bool INT8>
+__device__ __forceinline__ void step_update(const DecodeParams& p, const int b, const int kvh, const int ctx,
+                                            const int id) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pos = ctx - 1, off = pos % p.bs;
+    const int slot = (INT8 && p.slots) ? p.slots[b] : -1;
+    const bool ok = INT8 ? (slot >= 0 && slot < p.max_slots) : (id >= 0);
+    if (ok) {
+        const size_t row = INT8 ? (size_t(slot) * p.Hkv + kvh) * p.bs + off : (size_t(id) * p.Hkv + kvh) * p.bs + off;
+        uint16_t* dk = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.k_tail : p.k_pool)) + row * D;
+        uint16_t* dv = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.v_tail : p.v_pool)) + row * D;
+        const uint16_t* sk = p.k_new + (size_t(b) * p.Hkv + kvh) * D;
+        const uint16_t* sv = p.v_new + (size_t(b) * p.Hkv + kvh) * D;
+        for (int c = tid; c < 2 * (D / 8); c += kThreads) {
+            const int kv = c / (D / 8), ch = c % (D / 8);
+            *reinterpret_cast<uint4*>((kv ? dv : dk) + ch * 8) = ldg128((kv ? sv : sk) + ch * 8);
+        }
+        if (!INT8) fence_proxy_async_global();  // the pool row is read by a bulk copy later
+    } else if (tid == 0) {
+        report(p.err, INT8 ? kErrSlot : kErrBlockId);
+    }
+    __syncthreads();
+    if (INT8 && ok && (pos + 1) % p.bs == 0) {
+        if (id >= 0) {
+            for (int kv = warp; kv < 2; kv += kWarps) {  // K slab, V slab
+                const uint16_t* src = static_cast<const uint16_t*>(kv ? p.v_tail : p.k_tail) +
+                                      (size_t(slot) * p.Hkv + kvh) * p.bs * D;
+                int8_t* dst = static_cast<int8_t*>(const_cast<void*>(kv ? p.v_pool : p.k_pool)) +
+                              (size_t(id) * p.Hkv + kvh) * p.bs * D;
+                quantize_slab<D, true>(lane, src, D, p.bs, dst,
+                                       const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + kv);
+                fence_proxy_async_global();  // the codes are read by a bulk copy later
+            }
+        } else if (tid == 0) {
+            report(p.err, kErrBlockId);
+        }
+        __syncthreads();
+    }
+}
+
+// How a unit ended: the warp's tile count so far, whether the mbarriers are
+// initialised, and whether the next unit's table and first tiles are in place.
+struct UnitEnd {
+    int kb;
+    bool inited;
+    bool preissued;
+};
+
 // One unit of decode work: kv head kvh of sequence b over tokens [t0, t1) --
 // split j of ns (SEG: the unit's own range and count; else split blockIdx.x of
 // the context cut every split_tokens). kb: tiles this warp has consumed in
 // earlier units of the CTA (ring stage and mbarrier phase continue from it);
-// init: the mbarriers still need initialising. Returns the updated count, or
-// its complement (negative) when the unit ended before initialising them.
+// init: the mbarriers still need initialising. SEG only: tb = which of the
+// two table buffers is this unit's; preissued = the previous unit already
+// loaded this unit's table and scales and issued its first tiles; nxt = the
+// next unit's entry (nxt.x < 0: none), whose table and scales this unit
+// loads and whose first tiles it issues before its own epilogue, so that the
+// ring keeps streaming across the unit boundary.
 template <int D, int G, bool INT8, bool SPLIT, bool SEG>
-__device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem, const int b, const int kvh,
-                                            const int j, const int seg_t0, const int seg_t1, const int seg_ns,
-                                            const bool init, const int kb) {
+__device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* smem, const int b, const int kvh,
+                                               const int j, const int seg_t0, const int seg_t1, const int seg_ns,
+                                               const bool init, const int kb, const int tb, const bool preissued,
+                                               const int4 nxt) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
     static_assert(SPLIT || !SEG, "work-list units are splits");
     using T = DecodeTraits<D, INT8>;
@@ -463,13 +521,20 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
     constexpr int STAGES = T::kStages;
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
-    int32_t* tab = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
-    float2* bsc = reinterpret_cast<float2*>(tab + p.tab_cap);
-    // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2] sit in its own
-    // ring, free once its last tile has been consumed.
+    // SEG: two table / scale buffers (this unit's and the next one's) and a
+    // merge space of its own; otherwise one table, and the merge reuses the rings
+    int32_t* tab_base = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
+    int32_t* tab = tab_base + (SEG ? tb * p.tab_cap : 0);
+    float2* bsc_base = reinterpret_cast<float2*>(tab_base + (SEG ? 2 : 1) * p.tab_cap);
+    float2* bsc = bsc_base + (SEG ? tb * p.tab_cap : 0);
+    float* mseg = reinterpret_cast<float*>(bsc_base + (SEG ? 2 * p.tab_cap : 0));
+    // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2] -- in its own
+    // ring (free once its last tile has been consumed), or in mseg (SEG).
     static_assert(G * D * 4 + G * 8 <= STAGES * T::kStageBytes, "merge space fits one warp's ring");
-    auto mo_of = [&](int w) { return reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes); };
-    auto mml_of = [&](int w) { return mo_of(w) + G * D; };
+    auto mo_of = [&](int w) {
+        return SEG ? mseg + w * G * D : reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes);
+    };
+    auto mml_of = [&](int w) { return SEG ? mseg + kWarps * G * D + w * G * 2 : mo_of(w) + G * D; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -486,7 +551,7 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
     }
     const int t0 = SEG ? seg_t0 : SPLIT ? j * p.split_tokens : 0;
     const int t1 = SEG ? min(ctx, seg_t1) : SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
-    if (t0 >= t1 && (SEG ? ctx > 0 : j > 0)) return init ? ~kb0 : kb0;  // past the context
+    if (t0 >= t1 && (SEG ? ctx > 0 : j > 0)) return UnitEnd{kb0, !init, false};  // past the context
 
     const int nfull = INT8 ? (ctx / p.bs) * p.bs : ctx;
     const int pool_end = min(t1, nfull);
@@ -494,9 +559,11 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
     const int nt = (npool + kTile - 1) / kTile;
     const int blk0 = t0 / p.bs;
     const int nblk = npool > 0 ? min((pool_end - 1) / p.bs - blk0 + 1, p.tab_cap) : 0;
-    const int last_blk = ctx > 0 ? (ctx - 1) / p.bs : 0;                       // may change this step
-    const int nt_stable = max(0, min(nt, (last_blk * p.bs - t0) / kTile));      // tiles below it
-    const int nblk_stable = max(0, min(nblk, last_blk - blk0));
+    // the block holding token ctx-1 may change this step (work lists: already
+    // updated at kernel start, so every tile is settled)
+    const int last_blk = ctx > 0 ? (ctx - 1) / p.bs : 0;
+    const int nt_stable = SEG ? nt : max(0, min(nt, (last_blk * p.bs - t0) / kTile));  // tiles below it
+    const int nblk_stable = SEG ? nblk : max(0, min(nblk, last_blk - blk0));
 
     const uint32_t bar0 = smem_addr(bars);
     const uint32_t stage0 = smem_addr(stages);
@@ -507,34 +574,37 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
 
     if ((!SEG || init) && lane == 0)
         for (int s = 0; s < STAGES; ++s) mbar_init(bar_of(s), 1);
+    const bool ready = SEG && preissued;  // table, scales and first tiles already in place
     const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks + blk0;
-    for (int i = tid; i < nblk; i += kThreads) {
-        int id = trow[i];
-        if (id < 0 || id >= p.num_blocks) {
-            report(p.err, kErrBlockId);
-            id = -1;
+    if (!ready)
+        for (int i = tid; i < nblk; i += kThreads) {
+            int id = trow[i];
+            if (id < 0 || id >= p.num_blocks) {
+                report(p.err, kErrBlockId);
+                id = -1;
+            }
+            tab[i] = id;
         }
-        tab[i] = id;
-    }
     fence_mbar_init();
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
-    auto issue = [&](int tile, int s) {
-        const int tok = t0 + tile * kTile;
-        const int id = tab[tok / p.bs - blk0];
+    auto issue_for = [&](const int32_t* tb_, int t0_, int blk0_, int kvh_, int tile, int s) {
+        const int tok = t0_ + tile * kTile;
+        const int id = tb_[tok / p.bs - blk0_];
         const uint32_t bar = bar_of(s);
         if (id < 0) {
             mbar_arrive(bar);
             return;
         }
-        const size_t row = (size_t(id) * p.Hkv + kvh) * p.bs + (tok % p.bs);
+        const size_t row = (size_t(id) * p.Hkv + kvh_) * p.bs + (tok % p.bs);
         const uint8_t* ks = static_cast<const uint8_t*>(p.k_pool) + row * T::kRowBytes;
         const uint8_t* vs = static_cast<const uint8_t*>(p.v_pool) + row * T::kRowBytes;
         mbar_arrive_expect_tx(bar, T::kStageBytes);
         bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
         bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
     };
+    auto issue = [&](int tile, int s) { issue_for(tab, t0, blk0, kvh, tile, s); };
     // block scales, copied asynchronously (waited for before the main loop)
     auto load_scales = [&](int lo, int hi) {
         for (int i = lo + tid; i < hi; i += kThreads) {
@@ -545,12 +615,45 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
                 bsc[i] = make_float2(0.f, 0.f);
         }
     };
-    if (lane == 0)
+    if (lane == 0 && !ready)
         for (int s = 0; s < STAGES; ++s) {
             const int tile = warp + s * kWarps;
             if (tile < nt_stable) issue(tile, (kb0 + s) % STAGES);
         }
-    if (INT8) load_scales(0, nblk_stable);
+    if (INT8 && !ready) load_scales(0, nblk_stable);
+
+    // SEG: the next unit's table and scales, into the other buffers
+    int nt_n = 0, t0_n = 0, blk0_n = 0, kvh_n = 0;
+    int32_t* tab_n = tab_base + (SEG ? (tb ^ 1) * p.tab_cap : 0);
+    if (SEG && nxt.x >= 0) {
+        const int b_n = nxt.x;
+        kvh_n = nxt.w & 0xFF;
+        t0_n = nxt.y;
+        int ctx_n = p.ctx_lens[b_n];
+        if (ctx_n < 0 || ctx_n > p.max_blocks * p.bs) ctx_n = 0;  // reported when the unit runs
+        const int t1_n = min(ctx_n, nxt.z);
+        const int pe_n = min(t1_n, INT8 ? (ctx_n / p.bs) * p.bs : ctx_n);
+        const int np_n = max(0, pe_n - t0_n);
+        nt_n = (np_n + kTile - 1) / kTile;
+        blk0_n = t0_n / p.bs;
+        const int nblk_n = np_n > 0 ? min((pe_n - 1) / p.bs - blk0_n + 1, p.tab_cap) : 0;
+        float2* bsc_n = bsc_base + (tb ^ 1) * p.tab_cap;
+        const int32_t* trow_n = p.block_tables + size_t(b_n) * p.max_blocks + blk0_n;
+        for (int i = tid; i < nblk_n; i += kThreads) {
+            int id = trow_n[i];
+            if (id < 0 || id >= p.num_blocks) {
+                report(p.err, kErrBlockId);
+                id = -1;
+            }
+            tab_n[i] = id;
+            if (INT8) {
+                if (id >= 0)
+                    cp_async8(smem_addr(bsc_n + i), p.scales + (size_t(id) * p.Hkv + kvh_n) * 2);
+                else
+                    bsc_n[i] = make_float2(0.f, 0.f);
+            }
+        }
+    }
 
     pdl_wait();  // the previous kernel (and so the previous layer) has completed
 
@@ -561,45 +664,11 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
 
     // ---- fused step update: the split holding token ctx-1 writes that token's
     // K/V row (given in k_new / v_new) and, in INT8 mode, quantizes its block if
-    // the row filled it -- before any read of that block.
-    if (p.k_new != nullptr && ctx > 0 && t0 <= ctx - 1 && ctx - 1 < t1) {
-        const int pos = ctx - 1, off = pos % p.bs;
-        const int bl = pos / p.bs - blk0;
-        const int id = (bl >= 0 && bl < nblk) ? tab[bl] : -1;
-        const int slot = (INT8 && p.slots) ? p.slots[b] : -1;
-        const bool ok = INT8 ? (slot >= 0 && slot < p.max_slots) : (id >= 0);
-        if (ok) {
-            const size_t row = INT8 ? (size_t(slot) * p.Hkv + kvh) * p.bs + off
-                                    : (size_t(id) * p.Hkv + kvh) * p.bs + off;
-            uint16_t* dk = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.k_tail : p.k_pool)) + row * D;
-            uint16_t* dv = static_cast<uint16_t*>(const_cast<void*>(INT8 ? p.v_tail : p.v_pool)) + row * D;
-            const uint16_t* sk = p.k_new + (size_t(b) * p.Hkv + kvh) * D;
-            const uint16_t* sv = p.v_new + (size_t(b) * p.Hkv + kvh) * D;
-            for (int c = tid; c < 2 * (D / 8); c += kThreads) {
-                const int kv = c / (D / 8), ch = c % (D / 8);
-                *reinterpret_cast<uint4*>((kv ? dv : dk) + ch * 8) = ldg128((kv ? sv : sk) + ch * 8);
-            }
-            if (!INT8) fence_proxy_async_global();  // the pool row is read by a bulk copy below
-        } else if (tid == 0) {
-            report(p.err, INT8 ? kErrSlot : kErrBlockId);
-        }
-        __syncthreads();
-        if (INT8 && ok && (pos + 1) % p.bs == 0) {
-            if (id >= 0) {
-                for (int kv = warp; kv < 2; kv += kWarps) {  // K slab, V slab
-                    const uint16_t* src = static_cast<const uint16_t*>(kv ? p.v_tail : p.k_tail) +
-                                          (size_t(slot) * p.Hkv + kvh) * p.bs * D;
-                    int8_t* dst = static_cast<int8_t*>(const_cast<void*>(kv ? p.v_pool : p.k_pool)) +
-                                  (size_t(id) * p.Hkv + kvh) * p.bs * D;
-                    quantize_slab<D, true>(lane, src, D, p.bs, dst,
-                                           const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + kv);
-                    fence_proxy_async_global();  // the codes are read by a bulk copy below
-                }
-            } else if (tid == 0) {
-                report(p.err, kErrBlockId);
-            }
-            __syncthreads();
-        }
+    // the row filled it -- before any read of that block. (Work lists do this
+    // for all of a CTA's units at kernel start.)
+    if (!SEG && p.k_new != nullptr && ctx > 0 && t0 <= ctx - 1 && ctx - 1 < t1) {
+        const int bl = (ctx - 1) / p.bs - blk0;
+        step_update<D, INT8>(p, b, kvh, ctx, (bl >= 0 && bl < nblk) ? tab[bl] : -1);
     }
 
     if (lane == 0)
@@ -689,6 +758,17 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
             (void)wait_phase(bar_of((kb0 + kk) % STAGES), uint32_t((kb0 + kk) / STAGES) & 1u);
     }
     const int kbn = kb0 + k;
+    // SEG: this warp's ring is empty -- start the next unit's first tiles now,
+    // so that they stream during this unit's merge and epilogue (its table was
+    // written before the barrier ahead of the main loop)
+    if (SEG && nxt.x >= 0 && lane == 0) {
+        fence_proxy_async_smem();
+        for (int s = 0; s < STAGES; ++s) {
+            const int tile = warp + s * kWarps;
+            if (tile < nt_n) issue_for(tab_n, t0_n, blk0_n, kvh_n, tile, (kbn + s) % STAGES);
+        }
+    }
+    const UnitEnd done{kbn, true, SEG && nxt.x >= 0};
 
     // ---- merge: lanes of a warp hold disjoint dims; sum l over the 8 g lanes
 #pragma unroll
@@ -719,7 +799,7 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
         // no tokens: a zero row (no partials, no counter)
         for (int e = tid; e < G * D; e += kThreads)
             reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G) * D + e] = __float2bfloat16_rn(0.f);
-        return kbn;
+        return done;
     }
     // With the fused merge, a sequence whose context fits one split has
     // nothing to merge: its only split writes the output itself.
@@ -758,11 +838,14 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
         __syncthreads();
         if (tid == 0) s_last = atom_add_acq_rel_gpu(cnt, 1) == ns - 1;
         __syncthreads();
-        if (!s_last) return kbn;
+        if (!s_last) return done;
         constexpr int EPT = (G * D + kThreads - 1) / kThreads;  // output elements per thread
         constexpr int QB = EPT >= 48 ? 1 : 48 / EPT;   // splits per batch of loads
-        float* wsm = reinterpret_cast<float*>(stages);  // [G][ns] weights, then [G] sums
-        const bool staged = size_t(G) * ns + G <= size_t(kWarps) * STAGES * T::kStageBytes / 4;
+        // [G][ns] weights, then [G] sums: in the rings, or (SEG: the rings hold
+        // the next unit's tiles) in the merge space
+        float* wsm = SEG ? mseg : reinterpret_cast<float*>(stages);
+        const bool staged = size_t(G) * ns + G <= (SEG ? size_t(kWarps) * G * (D + 2)
+                                                       : size_t(kWarps) * STAGES * T::kStageBytes / 4);
         // first batch of partial outputs: issued before the weights are known
         float ov[QB][EPT];
         auto load_o = [&](int q0) {
@@ -839,7 +922,7 @@ __device__ __forceinline__ int decode_unit(const DecodeParams& p, uint8_t* smem,
         }
         if (tid == 0) *cnt = 0;  // ready for the next call
     }
-    return kbn;
+    return done;
 }
 
 // Grid (split, kv head, sequence): one unit per CTA.
@@ -847,7 +930,8 @@ template <int D, int G, bool INT8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
-    (void)decode_unit<D, G, INT8, SPLIT, false>(p, smem, blockIdx.z, blockIdx.y, blockIdx.x, 0, 0, 0, true, 0);
+    (void)decode_unit<D, G, INT8, SPLIT, false>(p, smem, blockIdx.z, blockIdx.y, blockIdx.x, 0, 0, 0, true, 0, 0,
+                                                false, make_int4(-1, 0, 0, 0));
 }
 
 // Work list: CTA c runs units seg_offsets[c] .. seg_offsets[c+1]-1 of segs,
@@ -859,25 +943,48 @@ template <int D, int G, bool INT8>
 __global__ void __launch_bounds__(kThreads, kMinCtas) decode_segments_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
-    int kb = 0;
     const int lo = p.seg_offsets[blockIdx.x], hi = p.seg_offsets[blockIdx.x + 1];
-    bool init = true;
-    for (int i = lo; i < hi; ++i) {
-        const int4 sg = __ldg(reinterpret_cast<const int4*>(p.segs) + i);
+    const int4* segs = reinterpret_cast<const int4*>(p.segs);
+    auto valid = [&](const int4 sg) {
         const int b = sg.x, kvh = sg.w & 0xFF, j = (sg.w >> 8) & 0xFFF, ns = (sg.w >> 20) & 0xFFF;
-        if (b < 0 || b >= p.B || kvh >= p.Hkv || j >= ns || ns > p.max_splits || sg.y < 0 || sg.y > sg.z ||
-            (sg.y % kTile) != 0) {
+        return b >= 0 && b < p.B && kvh < p.Hkv && j < ns && ns <= p.max_splits && sg.y >= 0 && sg.y <= sg.z &&
+               (sg.y % kTile) == 0;
+    };
+    pdl_wait();  // the previous kernel (and so the previous layer) has completed
+    // the step updates of all this CTA's units first: every bulk copy after
+    // this point reads settled blocks, so units can prefetch one another's
+    if (p.k_new != nullptr)
+        for (int i = lo; i < hi; ++i) {
+            const int4 sg = __ldg(segs + i);
+            if (!valid(sg)) continue;
+            const int ctx = p.ctx_lens[sg.x];
+            if (ctx <= 0 || ctx > p.max_blocks * p.bs || sg.y > ctx - 1 || ctx - 1 >= sg.z) continue;
+            const int blk = (ctx - 1) / p.bs;
+            int id = p.block_tables[size_t(sg.x) * p.max_blocks + blk];
+            if (id < 0 || id >= p.num_blocks) id = -1;
+            step_update<D, INT8>(p, sg.x, sg.w & 0xFF, ctx, id);
+        }
+    int kb = 0, tb = 0;
+    bool init = true, pre = false;
+    for (int i = lo; i < hi; ++i) {
+        const int4 sg = __ldg(segs + i);
+        if (!valid(sg)) {
             if (threadIdx.x == 0) report(p.err, kErrSegment);
+            pre = false;
             continue;
         }
-        const int r = decode_unit<D, G, INT8, true, true>(p, smem, b, kvh, j, sg.y, sg.z, ns, init, kb);
-        if (r < 0) {
-            kb = ~r;
-        } else {
-            kb = r;
-            init = false;
+        int4 nx = make_int4(-1, 0, 0, 0);
+        if (i + 1 < hi) {
+            nx = __ldg(segs + i + 1);
+            if (!valid(nx)) nx.x = -1;
         }
-        __syncthreads();  // the next unit reuses the table, ring and merge space
+        const UnitEnd e = decode_unit<D, G, INT8, true, true>(p, smem, sg.x, sg.w & 0xFF, (sg.w >> 8) & 0xFFF, sg.y,
+                                                              sg.z, (sg.w >> 20) & 0xFFF, init, kb, tb, pre, nx);
+        kb = e.kb;
+        init = init && !e.inited;
+        pre = e.preissued;
+        tb ^= 1;
+        __syncthreads();  // the next unit reuses the table buffers and the merge space
     }
 }
 

@@ -263,6 +263,15 @@ static size_t decode_smem(int d, bool int8, int tab_cap) {
     return fixed + size_t(tab_cap) * (int8 ? 12 : 4);
 }
 
+// Work-list CTAs: two tables and two scale buffers (this unit's and the
+// next one's) and a merge space of their own ([warps][G][d] + [warps][G][2]).
+static size_t decode_smem_seg(int d, int g, bool int8, int tab_cap) {
+    size_t fixed = 0;
+    if (d == 64) fixed = int8 ? decode_smem_fixed<64, true>() : decode_smem_fixed<64, false>();
+    else fixed = int8 ? decode_smem_fixed<128, true>() : decode_smem_fixed<128, false>();
+    return fixed + size_t(tab_cap) * 2 * (4 + 8) + size_t(kWarps) * g * (size_t(d) + 2) * 4;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -458,7 +467,7 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
         tab_cap = std::min<int64_t>(max_blocks, int64_t(plan->max_unit_tokens) / c->block_size + 2);
         tab_cap += tab_cap & 1;
     }
-    const size_t smem = decode_smem(c->head_dim, int8, tab_cap);
+    const size_t smem = plan ? decode_smem_seg(c->head_dim, g, int8, tab_cap) : decode_smem(c->head_dim, int8, tab_cap);
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
     DecodeParams p;
