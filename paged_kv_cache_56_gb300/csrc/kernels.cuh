@@ -544,12 +544,18 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
     // step writes: context lengths, block tables, slots, and the blocks (and
     // scales) below the one holding token ctx-1 -- the only block this step's
     // append / quantize-on-fill may have written.
+    const int t0 = SEG ? seg_t0 : SPLIT ? j * p.split_tokens : 0;
+    // the first table entry of each thread is loaded together with the
+    // context length (the table row starts at t0, known without it), so the
+    // two reads cost one round trip instead of two
+    const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks + t0 / p.bs;
+    const bool ready = SEG && preissued;  // table, scales and first tiles already in place
+    const int id_first = (!ready && t0 / p.bs + tid < p.max_blocks && tid < p.tab_cap) ? trow[tid] : -1;
     int ctx = p.ctx_lens[b];
     if (ctx < 0 || ctx > p.max_blocks * p.bs) {
         if (tid == 0 && j == 0) report(p.err, kErrCtxLen);
         ctx = 0;
     }
-    const int t0 = SEG ? seg_t0 : SPLIT ? j * p.split_tokens : 0;
     const int t1 = SEG ? min(ctx, seg_t1) : SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
     if (t0 >= t1 && (SEG ? ctx > 0 : j > 0)) return UnitEnd{kb0, !init, false};  // past the context
 
@@ -574,11 +580,9 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
 
     if ((!SEG || init) && lane == 0)
         for (int s = 0; s < STAGES; ++s) mbar_init(bar_of(s), 1);
-    const bool ready = SEG && preissued;  // table, scales and first tiles already in place
-    const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks + blk0;
     if (!ready)
         for (int i = tid; i < nblk; i += kThreads) {
-            int id = trow[i];
+            int id = i == tid ? id_first : trow[i];
             if (id < 0 || id >= p.num_blocks) {
                 report(p.err, kErrBlockId);
                 id = -1;
