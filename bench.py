@@ -317,7 +317,7 @@ def run_device(args, wl, rank, world):
     from paged_kv_cache_56_gb300.runtime import GraphStep
 
     device = f"cuda:{torch.cuda.current_device()}"
-    steps_total = args.warmup + args.steps + args.e2e_steps
+    steps_total = args.warmup + args.steps + args.e2e_steps + (2 if args.e2e_steps else 0)
     bench = Bench(wl, device, steps_total, split=args.split, fused_merge=not args.separate_merge)
     L, R, B = wl["L"], wl["repeat"], wl["B"]
     Hq, Hkv, d, bs = wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
@@ -389,17 +389,28 @@ def run_device(args, wl, rank, world):
     if err:
         raise RuntimeError(f"device error bits {err}")
 
-    # e2e: the same steps through host (pinned) buffers: H2D of the step's
-    # q/k/v into the graph's inputs, the step, D2H of the outputs -- all
-    # inside the timed region.
+    # e2e: the same steps through host (pinned) buffers: every step's q/k/v
+    # go host -> device and its outputs device -> host inside the timed region.
+    # With graphs the runtime's PipelinedSteps overlaps one step's transfers
+    # with its neighbours' compute (two untimed steps first capture its two
+    # graphs); eagerly, each step copies in, runs and copies out in turn.
     e2e = None
     if args.e2e_steps > 0:
+        from paged_kv_cache_56_gb300.runtime import PipelinedSteps
         base = args.warmup + args.steps
+        warm = 2 if graph else 0
         host_in = []
-        for s in range(args.e2e_steps):
+        for s in range(args.e2e_steps + warm):
             q, k, v = bench.step_inputs(base + s)
             host_in.append(tuple(t.cpu().pin_memory() for t in (q, k, v)))
-        hout = torch.empty(gs.out.shape, dtype=gs.out.dtype).pin_memory()
+        houts = [torch.empty(gs.out.shape, dtype=gs.out.dtype).pin_memory() for _ in range(2)]
+        pipe = None
+        if graph:
+            pipe = PipelinedSteps(bench.cache, B, bench.bufs.split_tokens, bench.sm_scale, R,
+                                  fused_merge=not args.separate_merge)
+            for s in range(warm):
+                pipe.step(bench.reqs, *host_in[s], houts[s % 2])
+            pipe.finish()
         e_ctx = []
         if world > 1:
             torch.distributed.barrier()
@@ -407,9 +418,14 @@ def run_device(args, wl, rank, world):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record()
         for s in range(args.e2e_steps):
-            plan = bench.step(gs, *host_in[s], graph)
-            hout.copy_(gs.out, non_blocking=True)
+            if pipe is not None:
+                plan = pipe.step(bench.reqs, *host_in[warm + s], houts[s % 2])
+            else:
+                plan = bench.step(gs, *host_in[s], graph)
+                houts[0].copy_(gs.out, non_blocking=True)
             e_ctx.append(plan.ctx_lens.copy())
+        if pipe is not None:
+            pipe.finish()
         t1.record()
         torch.cuda.synchronize()
         e_ms = max_over_ranks(t0.elapsed_time(t1), world)
@@ -417,7 +433,7 @@ def run_device(args, wl, rank, world):
         h2d = sum(t.numel() * t.element_size() for t in host_in[0])
         e2e = {"value": round(job_gbs(e_bytes, world, e_ms), 2), "unit": "GB/s",
                "tokens_per_s": round(B * world * args.e2e_steps / (e_ms * 1e-3), 1),
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(houts[0].numel() * houts[0].element_size()),
                "ms_per_step": round(e_ms / args.e2e_steps, 4)}
     return dict(ms=ms, attn_call_ms=attn_call_ms, attn_bytes=attn_bytes, step_bytes=step_bytes, clocks=clk,
                 launches=launches, split=bench.split, ctx=(int(ctx_hist[0].min()), int(ctx_hist[-1].max())),

@@ -486,3 +486,80 @@ class GraphStep:
 
     def replay(self) -> None:
         self.graph.replay()
+
+
+class PipelinedSteps:
+    """Decode steps fed from host memory with the transfers hidden behind
+    compute: two sets of step buffers, each with its own captured step graph,
+    take turns. Step s uploads its control arrays and its q / k / v on one
+    copy stream while step s-1 computes, and returns its outputs to the host
+    on a second copy stream (so that the next upload never queues behind a
+    return) while step s+1 computes. The steps themselves run in
+    order on the caller's stream, so the results are those of GraphStep step
+    by step. The first use of each set runs eagerly and captures its graph."""
+
+    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int, sm_scale: float, repeat: int = 1,
+                 fused_merge: bool = True):
+        self.cache, self.sm_scale, self.R = cache, sm_scale, repeat
+        self.sets = [StepBuffers(cache, max_batch, split_tokens, fused_merge) for _ in range(2)]
+        self.graphs = [None, None]
+        self.copy = torch.cuda.Stream(device=cache.device)      # host -> device
+        self.back = torch.cuda.Stream(device=cache.device)      # device -> host
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]     # a set's inputs are on the device
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]      # a set's step has run
+        self.returned = [torch.cuda.Event(), torch.cuda.Event()]  # a set's outputs are on the host
+        for e in self.done + self.returned:
+            e.record()
+        self.n = 0
+
+    def step(self, req_ids, q, k, v, out=None) -> StepPlan:
+        """One decode step. q [L*R, B, Hq, d], k / v [L, B, Hkv, d]: pinned host
+        (or device) bf16; out: pinned host bf16 [L*R, B, Hq, d] that receives
+        the step's outputs, or None to leave them in ``last_out()``. Host
+        buffers must stay untouched until ``finish()`` (or until the same set
+        comes round again, two steps later)."""
+        i = self.n & 1
+        bufs = self.sets[i]
+        compute = torch.cuda.current_stream()
+        plan = self.cache.plan_step(req_ids)
+        self.cache.apply_cow(plan, compute)
+        with torch.cuda.stream(self.copy):
+            self.copy.wait_event(self.done[i])      # the set's previous step has read its buffers
+            self.copy.wait_event(self.returned[i])  # ... and its outputs have left
+            bufs.upload(plan)
+            gs = self.graphs[i]
+            if gs is None:
+                gs = GraphStep(self.cache, bufs, self.sm_scale, self.R)
+            gs.q.copy_(q, non_blocking=True)
+            gs.k.copy_(k, non_blocking=True)
+            gs.v.copy_(v, non_blocking=True)
+            self.ready[i].record(self.copy)
+        compute.wait_event(self.ready[i])
+        if self.graphs[i] is None:
+            gs.run_eager()
+            self.graphs[i] = gs
+            self.done[i].record(compute)
+            gs.capture()  # synchronises: the eager step is complete
+        else:
+            gs.replay()
+            self.done[i].record(compute)
+        if out is not None:
+            with torch.cuda.stream(self.back):
+                self.back.wait_event(self.done[i])
+                out.copy_(gs.out, non_blocking=True)
+                self.returned[i].record(self.back)
+        self.cache.commit_step(req_ids)
+        self.last = i
+        self.n += 1
+        return plan
+
+    def last_out(self) -> torch.Tensor:
+        """Device outputs of the latest step (valid on the caller's stream)."""
+        return self.graphs[self.last].out
+
+    def finish(self) -> None:
+        """Makes the caller's stream wait for every transfer issued so far."""
+        for st in (self.copy, self.back):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            torch.cuda.current_stream().wait_event(ev)

@@ -193,3 +193,28 @@ def test_mixed_precision_layers(graph):
     for layer in range(4):
         for i in range(w.B):
             w.check_pool_bytes(layer, i, w.prior[i] + 18)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_pipelined_host_steps_equal_graph_steps(int8):
+    """PipelinedSteps (inputs from pinned host memory on a copy stream, two
+    alternating captured graphs, outputs back to pinned host memory) gives the
+    same bytes as GraphStep replays, step by step."""
+    from paged_kv_cache_56_gb300 import synth
+    from paged_kv_cache_56_gb300.runtime import PipelinedSteps
+    ref = Workload(seed=13, prior=(1, 17, 33, 100), int8=int8, split_tokens=32, max_blocks=9, graph=True, **TINY)
+    want = [ref.step().cpu() for _ in range(20)]
+    w = Workload(seed=13, prior=(1, 17, 33, 100), int8=int8, split_tokens=32, max_blocks=9, graph=True, **TINY)
+    pipe = PipelinedSteps(w.cache, w.B, w.split_tokens, w.sm_scale)
+    outs = [torch.empty((1, w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory() for _ in range(20)]
+    for t in range(20):
+        pos = torch.tensor([w.cache.seqs[r].length for r in w.req_ids], dtype=torch.int64)
+        q = w.q(0, t, w.req_ids)[None].cpu().pin_memory()
+        k = w.kv(0, synth.KIND_K, w.req_ids, pos)[None].cpu().pin_memory()
+        v = w.kv(0, synth.KIND_V, w.req_ids, pos)[None].cpu().pin_memory()
+        pipe.step(w.req_ids, q, k, v, outs[t])
+    pipe.finish()
+    torch.cuda.synchronize()
+    for t in range(20):
+        assert torch.equal(outs[t], want[t]), t
+    assert w.error_bits() == 0
