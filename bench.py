@@ -314,10 +314,10 @@ def job_gbs(bytes_per_rank: float, world: int, ms: float) -> float:
 
 
 def run_device(args, wl, rank, world):
-    from paged_kv_cache_56_gb300.runtime import GraphStep
+    from paged_kv_cache_56_gb300.runtime import GraphStep, PipelinedSteps
 
     device = f"cuda:{torch.cuda.current_device()}"
-    steps_total = args.warmup + args.steps + args.e2e_steps + (2 if args.e2e_steps else 0)
+    steps_total = args.warmup + args.steps + args.e2e_steps
     bench = Bench(wl, device, steps_total, split=args.split, fused_merge=not args.separate_merge)
     L, R, B = wl["L"], wl["repeat"], wl["B"]
     Hq, Hkv, d, bs = wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
@@ -326,8 +326,17 @@ def run_device(args, wl, rank, world):
     pkv.pkv_set_programmatic_launch(not args.no_pdl)
     # inputs for every step, resident in HBM before timing
     inputs = [bench.step_inputs(s) for s in range(args.warmup + args.steps)]
-    gs = None
+    # Graphs: the runtime's PipelinedSteps (control uploads and input copies on
+    # a copy stream, two alternating captured step graphs; the first warm-up
+    # steps capture them). Eager: one GraphStep run kernel by kernel.
+    pipe = gs = None
+    if graph:
+        pipe = PipelinedSteps(bench.cache, B, bench.split, bench.sm_scale, R, fused_merge=not args.separate_merge)
+    run = (lambda s, q, k, v, out=None: pipe.step(bench.reqs, q, k, v, out)) if graph else None
     for s in range(args.warmup):
+        if graph:
+            run(s, *inputs[s])
+            continue
         if gs is None:
             plan = bench.cache.plan_step(bench.reqs)
             bench.bufs.upload(plan)
@@ -338,10 +347,10 @@ def run_device(args, wl, rank, world):
             gs.v.copy_(v)
             gs.run_eager()
             bench.cache.commit_step(bench.reqs)
-            if graph:
-                gs.capture()
         else:
-            bench.step(gs, *inputs[s], graph)
+            bench.step(gs, *inputs[s], False)
+    if graph:
+        pipe.finish()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device())
@@ -353,32 +362,33 @@ def run_device(args, wl, rank, world):
     torch.cuda.synchronize()
     start.record()
     for s in range(args.steps):
-        plan = bench.step(gs, *inputs[args.warmup + s], graph)
+        x = inputs[args.warmup + s]
+        plan = run(s, *x) if graph else bench.step(gs, *x, False)
         ctx_hist.append(plan.ctx_lens.copy())
+    if graph:
+        pipe.finish()
     stop.record()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    launches = gs.launches_per_step() * args.steps
+    last = pipe.graphs[pipe.last] if graph else gs
+    launches = last.launches_per_step() * args.steps
     ms = start.elapsed_time(stop)
 
     # roofline: the step's kernels alone (one pkv_decode_step per layer and
     # repeat), replayed back to back on the launching stream and timed with
-    # CUDA events. Re-running the last step's launches with unchanged control
-    # arrays is idempotent: the same row is rewritten and a block that filled
-    # is quantized again to the same bytes.
+    # CUDA events. Re-running the last step's launches with its unchanged
+    # control arrays is idempotent: the same row is rewritten and a block that
+    # filled is quantized again to the same bytes.
     attn_reps = max(3, min(200, int(200.0 / max(ms / args.steps, 1e-3))))
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if graph:
-        a0.record()
-        for _ in range(attn_reps):
-            gs.graph.replay()
-        a1.record()
-    else:
-        a0.record()
-        for _ in range(attn_reps):
-            gs._layers()
-        a1.record()
+    a0.record()
+    for _ in range(attn_reps):
+        if graph:
+            last.graph.replay()
+        else:
+            last._layers()
+    a1.record()
     torch.cuda.synchronize()
     clk = clocks.stop()
     attn_call_ms = a0.elapsed_time(a1) / (attn_reps * L * R)
@@ -389,28 +399,18 @@ def run_device(args, wl, rank, world):
     if err:
         raise RuntimeError(f"device error bits {err}")
 
-    # e2e: the same steps through host (pinned) buffers: every step's q/k/v
-    # go host -> device and its outputs device -> host inside the timed region.
-    # With graphs the runtime's PipelinedSteps overlaps one step's transfers
-    # with its neighbours' compute (two untimed steps first capture its two
-    # graphs); eagerly, each step copies in, runs and copies out in turn.
+    # e2e: the same steps through host (pinned) buffers: every step's q/k/v go
+    # host -> device and its outputs device -> host inside the timed region
+    # (with graphs, overlapped with the neighbouring steps' compute by
+    # PipelinedSteps; eagerly, each step copies in, runs and copies out).
     e2e = None
     if args.e2e_steps > 0:
-        from paged_kv_cache_56_gb300.runtime import PipelinedSteps
         base = args.warmup + args.steps
-        warm = 2 if graph else 0
         host_in = []
-        for s in range(args.e2e_steps + warm):
+        for s in range(args.e2e_steps):
             q, k, v = bench.step_inputs(base + s)
             host_in.append(tuple(t.cpu().pin_memory() for t in (q, k, v)))
-        houts = [torch.empty(gs.out.shape, dtype=gs.out.dtype).pin_memory() for _ in range(2)]
-        pipe = None
-        if graph:
-            pipe = PipelinedSteps(bench.cache, B, bench.bufs.split_tokens, bench.sm_scale, R,
-                                  fused_merge=not args.separate_merge)
-            for s in range(warm):
-                pipe.step(bench.reqs, *host_in[s], houts[s % 2])
-            pipe.finish()
+        houts = [torch.empty(last.out.shape, dtype=last.out.dtype).pin_memory() for _ in range(2)]
         e_ctx = []
         if world > 1:
             torch.distributed.barrier()
@@ -418,13 +418,13 @@ def run_device(args, wl, rank, world):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record()
         for s in range(args.e2e_steps):
-            if pipe is not None:
-                plan = pipe.step(bench.reqs, *host_in[warm + s], houts[s % 2])
+            if graph:
+                plan = run(s, *host_in[s], houts[s % 2])
             else:
-                plan = bench.step(gs, *host_in[s], graph)
+                plan = bench.step(gs, *host_in[s], False)
                 houts[0].copy_(gs.out, non_blocking=True)
             e_ctx.append(plan.ctx_lens.copy())
-        if pipe is not None:
+        if graph:
             pipe.finish()
         t1.record()
         torch.cuda.synchronize()
