@@ -218,3 +218,22 @@ def test_pipelined_host_steps_equal_graph_steps(int8):
     for t in range(20):
         assert torch.equal(outs[t], want[t]), t
     assert w.error_bits() == 0
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 64)], ids=["d64_bs16", "d128_bs64"])
+@pytest.mark.parametrize("split", [0, 64])
+def test_gqa_group_of_eight(int8, d, bs, split):
+    """The widest GQA group the kernels take (G = Hq / Hkv = 8, the MMA's full
+    N dimension), both head sizes and block sizes, with and without splits,
+    across block fills, against the oracle."""
+    w = Workload(seed=70 + d + bs, num_layers=1, prior=(3, 63, 64, 130), Hq=16, Hkv=2, d=d, bs=bs, num_blocks=40,
+                 int8=int8, split_tokens=split, max_blocks=5 if bs == 64 else 14)
+    for t in range(20):
+        out = w.step().float().cpu().numpy()
+        if t in (0, 1, 19):
+            for i in range(w.B):
+                assert_close(out[0, i], w.oracle_out(0, i, t), f"step {t} seq {i}")
+    assert w.error_bits() == 0
+    for i in range(w.B):
+        w.check_pool_bytes(0, i, w.prior[i] + 20)
