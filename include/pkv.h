@@ -364,6 +364,16 @@ size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
  * each other's launch and drain. */
 int pkv_set_programmatic_launch(int enable);
 
+/* Test hook for the bounded waits (no counterpart on the pages): with tile
+ * >= 0, decode launches issued afterwards leave the bulk copy of that tile of
+ * warp 0 of their first CTA unissued, so that warp's wait on it runs out
+ * (about a second), PKV_DEVERR_TIMEOUT is OR-ed into the error word, and the
+ * kernel drains its other copies (each wait again bounded) and returns --
+ * the GPU stays usable and later launches are unaffected. The outputs of the
+ * affected (sequence, kv head) are then meaningless. -1 (the default) turns
+ * it off. PKV_ERR_INVALID for tile < -1. Process-wide. */
+int pkv_debug_skip_copy(int32_t tile);
+
 /* Bytes of the library-owned split-K scratch array used by
  * pkv_decode_attention_static_ws (8 MiB, held on every GPU that loads the
  * library for the life of the process). */

@@ -138,6 +138,7 @@ static int check_desc(const pkv_cache_desc* c) {
 static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
 static std::atomic<int> g_pdl{0};
+static std::atomic<int> g_skip_copy{-1};
 
 // Copies whole slabs src[i] -> dst[i] for up to three arrays at once (slab
 // index * slab bytes = offset; arrays may be NULL): a0 and a1 with slabs of
@@ -280,6 +281,12 @@ extern "C" {
 
 int pkv_set_programmatic_launch(int enable) {
     g_pdl.store(enable ? 1 : 0);
+    return PKV_OK;
+}
+
+int pkv_debug_skip_copy(int32_t tile) {
+    if (tile < -1) return PKV_ERR_INVALID;
+    g_skip_copy.store(tile);
     return PKV_OK;
 }
 
@@ -498,6 +505,7 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     p.max_splits = split ? max_splits : 1;
     p.tab_cap = tab_cap;
     p.qscale = sm_scale * 1.4426950408889634f;
+    p.skip_copy = g_skip_copy.load(std::memory_order_relaxed);
     p.seg_offsets = plan ? plan->seg_offsets : nullptr;
     p.segs = plan ? plan->segs : nullptr;
     p.B = B;

@@ -51,7 +51,7 @@ EXPORTED = (
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
     "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step", "pkv_decode_layers",
     "pkv_fork", "pkv_cow_block", "pkv_block_refs", "pkv_copy_blocks", "pkv_copy_slots",
-    "pkv_plan_segments", "pkv_decode_layers_planned",
+    "pkv_plan_segments", "pkv_decode_layers_planned", "pkv_debug_skip_copy",
 )
 
 
@@ -121,6 +121,7 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.c_float, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
             "pkv_decode_ctas_per_sm": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _I32]),
             "pkv_set_programmatic_launch": (ctypes.c_int, [ctypes.c_int]),
+            "pkv_debug_skip_copy": (ctypes.c_int, [_I32]),
             "pkv_decode_layers": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _VP, _I64, _VP, _VP, _I64, _VP,
                                                  _I64, _VP, _I32, _VP, _VP, _I32, ctypes.c_float, _I32, _I32, _VP,
                                                  _VP, _VP, _VP]),
@@ -322,6 +323,12 @@ def pkv_quantize_blocks_from(desc: CacheDesc, k_src: torch.Tensor, v_src: torch.
     bp = _dev(block_ids, "block_ids", torch.int32, M)
     _check("pkv_quantize_blocks_from",
            lib().pkv_quantize_blocks_from(_desc_ptr(desc), kp, vp, bp, M, _stream(stream)))
+
+
+def pkv_debug_skip_copy(tile: int) -> None:
+    """Test hook: later decode launches leave one bulk copy unissued so that a
+    bounded wait runs out (PKV_DEVERR_TIMEOUT); -1 turns it off."""
+    _check("pkv_debug_skip_copy", lib().pkv_debug_skip_copy(tile))
 
 
 def pkv_set_programmatic_launch(enable: bool) -> None:

@@ -137,3 +137,26 @@ def test_quantize_special_cases_bit_exact(case):
     q_ref, s_ref = quantize_block(x)
     assert np.array_equal(q, q_ref)
     assert np.float32(s).view(np.uint32) == np.float32(s_ref).view(np.uint32)
+
+
+@pytest.mark.parametrize("split", [0, 32])
+def test_bounded_wait_runs_out_and_the_gpu_recovers(split):
+    """A bulk copy that is never issued (the library's test hook) makes its
+    bounded wait run out: the kernel reports PKV_DEVERR_TIMEOUT, drains its
+    other copies and returns, and the next step on the same cache is right."""
+    from harness import Workload
+    w = Workload(seed=23, num_layers=1, prior=(100, 17, 33, 1), Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=True,
+                 split_tokens=split, max_blocks=9)
+    pkv.pkv_debug_skip_copy(0)  # tile 0 of warp 0 of the first CTA: sequence 0 has pool tiles
+    try:
+        w.step()
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_debug_skip_copy(-1)
+    assert w.error_bits() & pkv.PKV_DEVERR_TIMEOUT
+    for lc in w.cache.layers:
+        lc.err.zero_()
+    out = w.step().float().cpu().numpy()  # the cache itself was written by the append kernels
+    for i in range(w.B):
+        assert_close(out[0, i], w.oracle_out(0, i, 1), f"seq {i}")
+    assert w.error_bits() == 0
