@@ -294,7 +294,7 @@ def run_trace(args, wl):
     if sum(lc.error_bits() for lc in cache.layers):
         raise RuntimeError("device error bits set")
     return dict(ms=ms, nbytes=nbytes, ntok=ntok, launches=launches, clocks=clk, split=split,
-                running=len(drv.running), finished=len(drv.finished))
+                running=len(drv.running), finished=len(drv.finished), pool=cache.stats())
 
 
 def max_over_ranks(ms: float, world: int) -> float:
@@ -543,7 +543,7 @@ def main():
                 "data": "synthetic (seeded counter-based generator)",
                 "config": {"workload": "trace", "desc": wl["desc"], "split_tokens": r["split"],
                            "timed": "decode kernels of each step (admission prefill excluded)",
-                           "running_at_end": r["running"], "finished": r["finished"]},
+                           "running_at_end": r["running"], "finished": r["finished"], "kv_pool_at_end": r["pool"]},
                 "tokens_per_s": round(r["ntok"] / (r["ms"] * 1e-3), 1),
                 "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
                              "frac": round(value / peak, 4), "traffic": None, "peak_kind": peak_kind},

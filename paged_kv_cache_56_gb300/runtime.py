@@ -192,6 +192,21 @@ class PagedKVCache:
     def table(self, req_id: int) -> list:
         return pkv.pkv_request_table(self.alloc, req_id)
 
+    def stats(self) -> dict:
+        """Pool occupancy ("vLLM核心概念" §3.5: blocks used of total): free and
+        used blocks, live sequences, and the tokens allocated but not yet
+        written (each sequence's tail-block waste, below one block)."""
+        free = pkv.pkv_num_free(self.alloc)
+        held = set()
+        waste = 0
+        for r, sq in self.seqs.items():
+            t = self.table(r)
+            held.update(t)
+            waste += len(t) * self.bs - sq.length
+        total = self.layers[0].num_blocks
+        return dict(blocks_total=total, blocks_free=free, blocks_used=total - free, blocks_referenced=len(held),
+                    sequences=len(self.seqs), tail_waste_tokens=waste)
+
     # -- one decode step -----------------------------------------------------
     def plan_step(self, req_ids, tables_out: np.ndarray | None = None) -> StepPlan:
         """Host part of one decode step: grows block lists where a new block

@@ -345,3 +345,25 @@ def test_plan_segments_covers_every_pair_once(L, granule):
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_plan_segments([100, 200], 2, 16, 8, 3)
     assert e.value.code == pkv.PKV_ERR_TOO_LARGE
+
+
+def test_cache_stats_count_blocks_and_tail_waste(L):
+    """Pool occupancy of the runtime: used + free = total, tail waste below one
+    block per sequence, shared prefix blocks counted once."""
+    import torch
+    from paged_kv_cache_56_gb300.runtime import PagedKVCache
+    c = PagedKVCache(2, 32, 4, 2, 64, 16, False, max_slots=4, max_blocks_per_seq=8, device="cpu")
+    try:
+        c.add_sequence(-1, 2)
+        prefix = c.table(-1)
+        c.seqs[-1].length = 32
+        c.add_sequence(7, 3, shared_blocks=prefix)
+        c.seqs[7].length = 2 * 16 + 40
+        c.add_sequence(8, 1, shared_blocks=prefix)
+        c.seqs[8].length = 2 * 16 + 1
+        st = c.stats()
+        assert st["blocks_total"] == 32 and st["blocks_used"] == 6 and st["blocks_free"] == 26
+        assert st["blocks_referenced"] == 6 and st["sequences"] == 3
+        assert st["tail_waste_tokens"] == (5 * 16 - 72) + (3 * 16 - 33)
+    finally:
+        c.close()
