@@ -15,7 +15,18 @@
 //     exactly to f16 in registers, and the per-block scales are applied to
 //     the scores and to the softmax weights, not per element;
 //   * fp32 online softmax in base 2 (scores pre-multiplied by log2 e); each
-//     warp keeps its own state, merged across warps through shared memory.
+//     warp keeps its own state, merged across warps through shared memory;
+//     with a bf16 cache the weights enter the PV product as two bf16 terms
+//     (rounded weight + residual);
+//   * the split holding token ctx-1 first appends that token's row and, when
+//     it fills a block, quantizes the block (the decode step fused into one
+//     kernel); the last split of a (sequence, kv head) to finish merges the
+//     splits' partial states (arrival counter), or a second kernel does;
+//   * under programmatic dependent launch the prologue (context length,
+//     block table, the first tiles below the block this step may write) runs
+//     before waiting for the previous kernel;
+//   * a work-list form runs a planned list of (sequence, kv head, token range)
+//     units per CTA back to back (decode_segments_kernel).
 #pragma once
 
 #include <cuda_bf16.h>
