@@ -367,3 +367,17 @@ def test_cache_stats_count_blocks_and_tail_waste(L):
         assert st["tail_waste_tokens"] == (5 * 16 - 72) + (3 * 16 - 33)
     finally:
         c.close()
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library the binding raises instead of falling back to
+    anything else (there is no CPU path)."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, {root!r});"
+            "from paged_kv_cache_56_gb300 import pkv; pkv.LIB_PATH = {missing!r}; pkv._lib = None\n"
+            "try:\n    pkv.lib()\nexcept RuntimeError as e:\n    print('raised', e)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code.format(root=root, missing=str(tmp_path / "libpkv.so"))],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.startswith("raised"), (r.stdout, r.stderr)
