@@ -52,7 +52,8 @@ extern "C" {
 #define PKV_ERR_EXISTS        -4  /* request id is already live */
 #define PKV_ERR_UNSUPPORTED   -5  /* shape outside the compiled set (see below) */
 #define PKV_ERR_CUDA          -6  /* a CUDA runtime call failed */
-#define PKV_ERR_TOO_LARGE     -7  /* the request needs more than the library's fixed scratch array */
+#define PKV_ERR_DEVICE_TIMEOUT -7 /* a kernel's bounded wait expired (pkv_sync_status) */
+#define PKV_ERR_TOO_LARGE     -8  /* the request needs more than the library's fixed scratch array */
 
 /* bits a kernel ORs into the descriptor's error word */
 #define PKV_DEVERR_BLOCK_ID    1  /* block id < 0 or >= num_blocks */
@@ -60,7 +61,6 @@ extern "C" {
 #define PKV_DEVERR_CTX_LEN     4  /* context length < 0 or > max_blocks * block_size */
 #define PKV_DEVERR_OFFSET      8  /* in-block offset < 0 or >= block_size */
 #define PKV_DEVERR_TIMEOUT    16  /* a bounded wait on an asynchronous copy expired */
-#define PKV_DEVERR_SEGMENT    32  /* a work-list entry out of range (pkv_decode_layers_planned) */
 
 #define PKV_DTYPE_BF16 0
 #define PKV_DTYPE_INT8 1
@@ -292,44 +292,6 @@ int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const voi
                       const int32_t* slots, int32_t B, float sm_scale, int32_t split_tokens,
                       int32_t max_splits, float* ws_o, float* ws_ml, int32_t* ws_count, void* stream);
 
-/* Work list for decode over sequences of very different lengths (a
- * continuous-batching step): pkv_plan_segments (host) lays the (sequence,
- * kv head) token runs of the step end to end, each rounded up to `granule`
- * tokens (a multiple of 16 and of block_size), and cuts them into num_ctas
- * pieces of equal length -- one wave of CTAs that start and finish
- * together. A piece is a list of units {b, t0, t1, kvh | j << 8 | ns << 20}:
- * tokens [t0, t1) of kv head kvh of sequence b, split j of the ns splits of
- * that pair (a sequence with ctx 0 gets one empty unit: its zero row).
- * Outputs: seg_offsets[num_ctas + 1] (piece c = units seg_offsets[c] ..
- * seg_offsets[c+1]-1), segs[seg_cap][4], info[4] = {units, most splits of one
- * pair, longest unit in tokens, pieces used}. PKV_ERR_TOO_LARGE when seg_cap
- * units do not suffice (or a pair would need more than 4095 splits);
- * PKV_ERR_INVALID for bad arguments (num_kv_heads must be < 256). Host memory
- * only; the caller copies seg_offsets and segs to the device. */
-int pkv_plan_segments(const int32_t* ctx_lens, int32_t B, int32_t num_kv_heads, int32_t granule,
-                      int32_t num_ctas, int32_t* seg_offsets, int32_t* segs, int32_t seg_cap, int32_t* info);
-
-typedef struct pkv_segment_plan {
-    const int32_t* seg_offsets;  /* device int32 [num_ctas + 1] */
-    const int32_t* segs;         /* device int32 [units][4], 16-byte aligned */
-    int32_t num_ctas;            /* CTAs to launch (pieces; unused pieces are empty) */
-    int32_t max_splits;          /* >= the most splits of one pair, <= 4095: the workspace's split extent */
-    int32_t max_unit_tokens;     /* >= the longest unit */
-} pkv_segment_plan;
-
-/* pkv_decode_layers over a work list instead of a uniform split: each of
- * plan->num_ctas CTAs runs its units back to back; the partial states of a
- * pair cut into several units are merged in the same kernel by the last one
- * to arrive (ws_count is required, zero before the first call and left at
- * zero; the workspace is sized for plan->max_splits). Same results as
- * pkv_decode_layers up to the order of the fp32 softmax merge. */
-int pkv_decode_layers_planned(const pkv_cache_desc* descs, int32_t num_layers, const void* q,
-                              int64_t q_layer_stride, const void* k_new, const void* v_new,
-                              int64_t kv_layer_stride, void* out, int64_t out_layer_stride,
-                              const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
-                              const int32_t* slots, int32_t B, float sm_scale, const pkv_segment_plan* plan,
-                              float* ws_o, float* ws_ml, int32_t* ws_count, void* stream);
-
 /* CTAs of the decode kernel for this cache shape that fit on one SM at once
  * (registers and shared memory), for a given split_tokens (0 = none) and
  * max_blocks; a caller sizes its splits so that B * Hkv * splits fills
@@ -351,6 +313,19 @@ int pkv_splitk_reduce(const float* ws_o, const float* ws_ml, const int32_t* ctx_
 size_t pkv_splitk_ws_o_bytes(int32_t B, int32_t Hq, int32_t head_dim, int32_t max_splits);
 size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
 
+/* Reads, clears and reports the error words of n descriptors once the work
+ * queued on `stream` has finished: synchronises the stream, copies each
+ * descriptor's err_word to the host (descriptors with a NULL err_word are
+ * skipped; descriptors may share one word), resets every nonzero word to 0
+ * on the stream, and writes the OR of the words to *out_bits (nullable).
+ * Returns PKV_ERR_DEVICE_TIMEOUT if PKV_DEVERR_TIMEOUT was set (a bounded
+ * wait of a kernel expired: its outputs are meaningless, later launches are
+ * unaffected), else PKV_ERR_INVALID if any other PKV_DEVERR_* bit was set (a
+ * block id, slot, context length or offset in device memory was out of range
+ * and skipped), else PKV_OK; PKV_ERR_CUDA if a CUDA call failed. Host-side,
+ * blocking; not for use inside stream capture. */
+int pkv_sync_status(const pkv_cache_desc* descs, int32_t n, void* stream, int32_t* out_bits);
+
 /* Process-wide switch (default off) for programmatic dependent launch: with
  * it on, every kernel of this library is launched so that it may start while
  * the previous kernel on the stream is still running, and each waits for that
@@ -365,13 +340,16 @@ size_t pkv_splitk_ws_ml_bytes(int32_t B, int32_t Hq, int32_t max_splits);
 int pkv_set_programmatic_launch(int enable);
 
 /* Test hook for the bounded waits (no counterpart on the pages): with tile
- * >= 0, decode launches issued afterwards leave the bulk copy of that tile of
- * warp 0 of their first CTA unissued, so that warp's wait on it runs out
- * (about a second), PKV_DEVERR_TIMEOUT is OR-ed into the error word, and the
- * kernel drains its other copies (each wait again bounded) and returns --
- * the GPU stays usable and later launches are unaffected. The outputs of the
+ * >= 0, decode launches issued afterwards run a separately compiled test
+ * build of the decode kernel (head_dim 64 only; other shapes then return
+ * PKV_ERR_UNSUPPORTED) that leaves the bulk copy of that tile of warp 0 of
+ * its first CTA unissued, so that warp's wait on it runs out (about a
+ * second), PKV_DEVERR_TIMEOUT is OR-ed into the error word, and the kernel
+ * drains its other copies (each wait again bounded) and returns -- the GPU
+ * stays usable and later launches are unaffected. The outputs of the
  * affected (sequence, kv head) are then meaningless. -1 (the default) turns
- * it off. PKV_ERR_INVALID for tile < -1. Process-wide. */
+ * it off and selects the regular kernels, which carry no such check.
+ * PKV_ERR_INVALID for tile < -1. Process-wide. */
 int pkv_debug_skip_copy(int32_t tile);
 
 /* Bytes of the library-owned split-K scratch array used by
@@ -396,8 +374,15 @@ int pkv_debug_skip_copy(int32_t tile);
  * 256 bytes; if that exceeds PKV_STATIC_WS_BYTES the call returns
  * PKV_ERR_TOO_LARGE and launches nothing.
  *
- * The first call on a device looks up the array's device address on that
- * device (the current one); make that first call before any stream capture.
+ * The array is part of the library's device code: it takes device memory when
+ * that code is loaded on a device -- with CUDA's lazy module loading, at the
+ * library's first kernel launch or first call of this function there. The
+ * first call on a device also looks up the array's device address on that
+ * device (the current one). Make that first call (or any launch of this
+ * library) on each device before the caller hands the device's free memory to
+ * a pool, and before any stream capture; after cudaDeviceReset the cached
+ * address is stale and the process must not call this function again.
+ * split_tokens < 0 returns PKV_ERR_INVALID.
  * Every call on a device shares the one array and it keeps the last call's
  * contents: each call first clears its counters (an asynchronous memset on
  * the stream), then writes its partials before reading them. Calls whose

@@ -13,7 +13,9 @@
 //   * QK and PV of each 16-token tile run on tensor cores (mma.m16n8k16,
 //     fp32 accumulate) straight from registers: INT8 codes are converted
 //     exactly to f16 in registers, and the per-block scales are applied to
-//     the scores and to the softmax weights, not per element;
+//     the scores and to the softmax weights, not per element; the weights of
+//     an INT8 block are kept inside f16's range by a per-warp power-of-two
+//     unit of the accumulator that follows the blocks' V scales;
 //   * fp32 online softmax in base 2 (scores pre-multiplied by log2 e); each
 //     warp keeps its own state, merged across warps through shared memory;
 //     with a bf16 cache the weights enter the PV product as two bf16 terms
@@ -24,12 +26,11 @@
 //     splits' partial states (arrival counter), or a second kernel does;
 //   * under programmatic dependent launch the prologue (context length,
 //     block table, the first tiles below the block this step may write) runs
-//     before waiting for the previous kernel;
-//   * a work-list form runs a planned list of (sequence, kv head, token range)
-//     units per CTA back to back (decode_segments_kernel).
+//     before waiting for the previous kernel.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -58,7 +59,6 @@ constexpr int kErrSlot = 2;
 constexpr int kErrCtxLen = 4;
 constexpr int kErrOffset = 8;
 constexpr int kErrTimeout = 16;
-constexpr int kErrSegment = 32;
 
 __device__ __forceinline__ void report(int32_t* err, int bits) {
     if (err) atomicOr(err, bits);
@@ -83,10 +83,7 @@ struct DecodeParams {
     int32_t* err;
     int32_t Hq, Hkv, bs, max_blocks, num_blocks, max_slots, split_tokens, max_splits;
     int32_t tab_cap;  // block-table entries the shared table holds (even)
-    const int32_t* seg_offsets;  // work list (decode_segments_kernel): [gridDim.x + 1]
-    const int32_t* segs;         // [n][4]
-    int32_t B;
-    int32_t skip_copy;  // >= 0: the first CTA's warp 0 never issues its tile of this index (timeout test)
+    int32_t skip_copy;  // test build only: the first CTA's warp 0 never issues its tile of this index
     float qscale;     // sm_scale * log2(e)
 };
 
@@ -225,19 +222,29 @@ __device__ __forceinline__ void load_run(const Rows& R, int r, int off, uint32_t
 
 // Per-warp online-softmax state: heads 2t and 2t+1 (replicated over g);
 // l is this lane's partial sum over its tokens; acc holds O^T fragments.
+// INT8 caches (SHIFT): the weights are taken against md = m - delta, i.e.
+// scaled by 2^delta, so that acc and l are kept in units of 2^-delta (see
+// kExpNone) and the weights times a block's V scale fit f16 whatever the
+// scale; otherwise md is unused and delta = 0.
 template <int D>
 struct WarpState {
-    float m[2], l[2];
+    float m[2], md[2], l[2];
     float acc[D / 16][4];
 };
 
+// 2^n as a float for -126 <= n <= 127.
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
+
 // One 16-token tile. nvalid < 16 masks the last rows: their scores become
 // -inf and their V values 0, so stale or uninitialised rows cannot leak NaNs.
-// hs[j]: log2-domain logit factor of head 2t+j; ksc/vsc: the block's scales.
-template <int D, bool I8, class Rows>
-__device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvalid, float ksc, float vsc,
-                                         const uint32_t (&qf)[D / 16][2], const float (&hs)[2], int g, int t,
-                                         WarpState<D>& st) {
+// hs[j]: log2-domain logit factor of head 2t+j; ksc: the block's K scale;
+// vmul: factor on the softmax weights before the PV product (the block's V
+// scale for INT8 tiles). SHIFT: weights against st.md (see WarpState), with
+// md kept at m - delta.
+template <int D, bool I8, bool SHIFT, class Rows>
+__device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvalid, float ksc, float vmul,
+                                         float delta, const uint32_t (&qf)[D / 16][2], const float (&hs)[2],
+                                         int g, int t, WarpState<D>& st) {
     using Gm = Geom<D, I8>;
     constexpr bool F16 = I8;
     // ---- S = K . Q^T (two independent accumulator chains, summed)
@@ -283,6 +290,10 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
         const float c0 = fast_exp2(st.m[0] - mx0), c1 = fast_exp2(st.m[1] - mx1);
         st.m[0] = mx0;
         st.m[1] = mx1;
+        if (SHIFT) {
+            st.md[0] = mx0 - delta;
+            st.md[1] = mx1 - delta;
+        }
         st.l[0] *= c0;
         st.l[1] *= c1;
 #pragma unroll
@@ -290,11 +301,12 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
             st.acc[m][0] *= c0; st.acc[m][1] *= c1; st.acc[m][2] *= c0; st.acc[m][3] *= c1;
         }
     }
-    const float p0 = fast_exp2(s[0] - st.m[0]), p1 = fast_exp2(s[1] - st.m[1]);
-    const float p2 = fast_exp2(s[2] - st.m[0]), p3 = fast_exp2(s[3] - st.m[1]);
+    const float r0 = SHIFT ? st.md[0] : st.m[0], r1 = SHIFT ? st.md[1] : st.m[1];
+    const float p0 = fast_exp2(s[0] - r0), p1 = fast_exp2(s[1] - r1);
+    const float p2 = fast_exp2(s[2] - r0), p3 = fast_exp2(s[3] - r1);
     st.l[0] += p0 + p2;
     st.l[1] += p1 + p3;
-    const float x0 = p0 * vsc, x1 = p1 * vsc, x2 = p2 * vsc, x3 = p3 * vsc;
+    const float x0 = p0 * vmul, x1 = p1 * vmul, x2 = p2 * vmul, x3 = p3 * vmul;
     const uint32_t w01 = pack2<F16>(x0, x1), w23 = pack2<F16>(x2, x3);
     const uint32_t b0 = movmatrix_t(w01), b1 = movmatrix_t(w23);
     // bf16 keeps 8 bits of a weight (a relative error up to 2^-9, visible when
@@ -503,73 +515,60 @@ __device__ __forceinline__ void step_update(const DecodeParams& p, const int b, 
     }
 }
 
-// How a unit ended: the warp's tile count so far, whether the mbarriers are
-// initialised, and whether the next unit's table and first tiles are in place.
-struct UnitEnd {
-    int kb;
-    bool inited;
-    bool preissued;
-};
+// INT8 caches keep the PV accumulators (and l) of a CTA in units of
+// 2^(ew - 14), where ew is the largest exponent among the V scales of the
+// CTA's blocks: a block's softmax weights enter the f16 product as
+// p * 2^(14 - ew) * vscale < 2^15, finite whatever the scales (the factor
+// 2^delta, delta = 14 - ew, is taken into the softmax's reference maximum, so
+// no tile pays a multiply for it). A block whose V scale is 2^k below the
+// largest keeps f16's normal range for weights p >= 2^(k - 28); smaller
+// weights of such a block lose relative precision (below 2^-24 of that
+// block's largest contribution, they flush to zero).
+constexpr int kExpNone = -1000;
 
-// One unit of decode work: kv head kvh of sequence b over tokens [t0, t1) --
-// split j of ns (SEG: the unit's own range and count; else split blockIdx.x of
-// the context cut every split_tokens). kb: tiles this warp has consumed in
-// earlier units of the CTA (ring stage and mbarrier phase continue from it);
-// init: the mbarriers still need initialising. SEG only: tb = which of the
-// two table buffers is this unit's; preissued = the previous unit already
-// loaded this unit's table and scales and issued its first tiles; nxt = the
-// next unit's entry (nxt.x < 0: none), whose table and scales this unit
-// loads and whose first tiles it issues before its own epilogue, so that the
-// ring keeps streaming across the unit boundary.
-template <int D, int G, bool INT8, bool SPLIT, bool SEG>
-__device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* smem, const int b, const int kvh,
-                                               const int j, const int seg_t0, const int seg_t1, const int seg_ns,
-                                               const bool init, const int kb, const int tb, const bool preissued,
-                                               const int4 nxt) {
+// Decode attention, one CTA per (split j = blockIdx.x, kv head = blockIdx.y,
+// sequence b = blockIdx.z). HOOK: the test build of pkv_debug_skip_copy, which
+// can leave one bulk copy unissued.
+template <int D, int G, bool INT8, bool SPLIT, bool HOOK>
+__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
-    static_assert(SPLIT || !SEG, "work-list units are splits");
     using T = DecodeTraits<D, INT8>;
     using Gm = Geom<D, INT8>;
     constexpr int STAGES = T::kStages;
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
+    const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
-    // SEG: two table / scale buffers (this unit's and the next one's) and a
-    // merge space of its own; otherwise one table, and the merge reuses the rings
-    int32_t* tab_base = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
-    int32_t* tab = tab_base + (SEG ? tb * p.tab_cap : 0);
-    float2* bsc_base = reinterpret_cast<float2*>(tab_base + (SEG ? 2 : 1) * p.tab_cap);
-    float2* bsc = bsc_base + (SEG ? tb * p.tab_cap : 0);
-    float* mseg = reinterpret_cast<float*>(bsc_base + (SEG ? 2 * p.tab_cap : 0));
-    // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2] -- in its own
-    // ring (free once its last tile has been consumed), or in mseg (SEG).
+    int32_t* tab = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
+    float2* bsc = reinterpret_cast<float2*>(tab + p.tab_cap);
+    // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2], in its own
+    // ring (free once its last tile has been consumed).
     static_assert(G * D * 4 + G * 8 <= STAGES * T::kStageBytes, "merge space fits one warp's ring");
-    auto mo_of = [&](int w) {
-        return SEG ? mseg + w * G * D : reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes);
-    };
-    auto mml_of = [&](int w) { return SEG ? mseg + kWarps * G * D + w * G * 2 : mo_of(w) + G * D; };
+    auto mo_of = [&](int w) { return reinterpret_cast<float*>(stages + size_t(w) * STAGES * T::kStageBytes); };
+    auto mml_of = [&](int w) { return mo_of(w) + G * D; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int kb0 = SEG ? kb : 0;
 
     // Before pdl_wait() this kernel reads only what no preceding kernel of the
     // step writes: context lengths, block tables, slots, and the blocks (and
     // scales) below the one holding token ctx-1 -- the only block this step's
     // append / quantize-on-fill may have written.
-    const int t0 = SEG ? seg_t0 : SPLIT ? j * p.split_tokens : 0;
+    const int t0 = SPLIT ? j * p.split_tokens : 0;
     // the first table entry of each thread is loaded together with the
     // context length (the table row starts at t0, known without it), so the
     // two reads cost one round trip instead of two
     const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks + t0 / p.bs;
-    const bool ready = SEG && preissued;  // table, scales and first tiles already in place
-    const int id_first = (!ready && t0 / p.bs + tid < p.max_blocks && tid < p.tab_cap) ? trow[tid] : -1;
+    const int id_first = (t0 / p.bs + tid < p.max_blocks && tid < p.tab_cap) ? trow[tid] : -1;
+    const int slot = (INT8 && p.slots) ? p.slots[b] : -1;
     int ctx = p.ctx_lens[b];
     if (ctx < 0 || ctx > p.max_blocks * p.bs) {
         if (tid == 0 && j == 0) report(p.err, kErrCtxLen);
         ctx = 0;
     }
-    const int t1 = SEG ? min(ctx, seg_t1) : SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
-    if (t0 >= t1 && (SEG ? ctx > 0 : j > 0)) return UnitEnd{kb0, !init, false};  // past the context
+    const int t1 = SPLIT ? min(ctx, t0 + p.split_tokens) : ctx;
+    if (t0 >= t1 && j > 0) return;  // past the context
 
     const int nfull = INT8 ? (ctx / p.bs) * p.bs : ctx;
     const int pool_end = min(t1, nfull);
@@ -577,51 +576,58 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
     const int nt = (npool + kTile - 1) / kTile;
     const int blk0 = t0 / p.bs;
     const int nblk = npool > 0 ? min((pool_end - 1) / p.bs - blk0 + 1, p.tab_cap) : 0;
-    // the block holding token ctx-1 may change this step (work lists: already
-    // updated at kernel start, so every tile is settled)
+    // the block holding token ctx-1 may change this step
     const int last_blk = ctx > 0 ? (ctx - 1) / p.bs : 0;
-    const int nt_stable = SEG ? nt : max(0, min(nt, (last_blk * p.bs - t0) / kTile));  // tiles below it
-    const int nblk_stable = SEG ? nblk : max(0, min(nblk, last_blk - blk0));
+    const int nt_stable = max(0, min(nt, (last_blk * p.bs - t0) / kTile));  // tiles below it
+    const int nblk_stable = max(0, min(nblk, last_blk - blk0));
+
+    // INT8: the largest V-scale exponent of the CTA's blocks, one slot per warp
+    __shared__ int s_ev[kWarps];
+    // exponent of a V scale (a positive normal float for every block the
+    // quantizer wrote; 0 marks a block id the table check dropped), clamped so
+    // that the powers of two built from it stay finite
+    auto v_exp = [](float v) {
+        const uint32_t u = __float_as_uint(v);
+        return u ? min(121, max(-40, int((u >> 23) & 0xFFu) - 127)) : kExpNone;
+    };
 
     const uint32_t bar0 = smem_addr(bars);
     const uint32_t stage0 = smem_addr(stages);
+    // this warp's k-th tile uses ring stage k % STAGES and waits for
+    // completion number k / STAGES of that stage's mbarrier
     auto bar_of = [&](int s) { return bar0 + uint32_t(warp * STAGES + s) * 8u; };
-    // this warp's i-th tile of the unit uses ring stage (kb + i) % STAGES, and
-    // waits for completion number (kb + i) / STAGES of that stage's mbarrier
     auto stage_of = [&](int s) { return stage0 + uint32_t(warp * STAGES + s) * T::kStageBytes; };
 
-    if ((!SEG || init) && lane == 0)
+    if (lane == 0)
         for (int s = 0; s < STAGES; ++s) mbar_init(bar_of(s), 1);
-    if (!ready)
-        for (int i = tid; i < nblk; i += kThreads) {
-            int id = i == tid ? id_first : trow[i];
-            if (id < 0 || id >= p.num_blocks) {
-                report(p.err, kErrBlockId);
-                id = -1;
-            }
-            tab[i] = id;
+    for (int i = tid; i < nblk; i += kThreads) {
+        int id = i == tid ? id_first : trow[i];
+        if (id < 0 || id >= p.num_blocks) {
+            report(p.err, kErrBlockId);
+            id = -1;
         }
+        tab[i] = id;
+    }
     fence_mbar_init();
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
-    auto issue_for = [&](const int32_t* tb_, int t0_, int blk0_, int kvh_, int tile, int s) {
-        const int tok = t0_ + tile * kTile;
-        const int id = tb_[tok / p.bs - blk0_];
+    auto issue = [&](int tile, int s) {
+        const int tok = t0 + tile * kTile;
+        const int id = tab[tok / p.bs - blk0];
         const uint32_t bar = bar_of(s);
-        if (tile == p.skip_copy && warp == 0 && blockIdx.x + blockIdx.y + blockIdx.z == 0) return;
+        if (HOOK && tile == p.skip_copy && warp == 0 && blockIdx.x + blockIdx.y + blockIdx.z == 0) return;
         if (id < 0) {
             mbar_arrive(bar);
             return;
         }
-        const size_t row = (size_t(id) * p.Hkv + kvh_) * p.bs + (tok % p.bs);
+        const size_t row = (size_t(id) * p.Hkv + kvh) * p.bs + (tok % p.bs);
         const uint8_t* ks = static_cast<const uint8_t*>(p.k_pool) + row * T::kRowBytes;
         const uint8_t* vs = static_cast<const uint8_t*>(p.v_pool) + row * T::kRowBytes;
         mbar_arrive_expect_tx(bar, T::kStageBytes);
         bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
         bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
     };
-    auto issue = [&](int tile, int s) { issue_for(tab, t0, blk0, kvh, tile, s); };
     // block scales, copied asynchronously (waited for before the main loop)
     auto load_scales = [&](int lo, int hi) {
         for (int i = lo + tid; i < hi; i += kThreads) {
@@ -632,43 +638,17 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
                 bsc[i] = make_float2(0.f, 0.f);
         }
     };
-    if (lane == 0 && !ready)
+    if (lane == 0)
         for (int s = 0; s < STAGES; ++s) {
             const int tile = warp + s * kWarps;
-            if (tile < nt_stable) issue(tile, (kb0 + s) % STAGES);
+            if (tile < nt_stable) issue(tile, s);
         }
-    if (INT8 && !ready) load_scales(0, nblk_stable);
-
-    // SEG: the next unit's table and scales, into the other buffers
-    int nt_n = 0, t0_n = 0, blk0_n = 0, kvh_n = 0;
-    int32_t* tab_n = tab_base + (SEG ? (tb ^ 1) * p.tab_cap : 0);
-    if (SEG && nxt.x >= 0) {
-        const int b_n = nxt.x;
-        kvh_n = nxt.w & 0xFF;
-        t0_n = nxt.y;
-        int ctx_n = p.ctx_lens[b_n];
-        if (ctx_n < 0 || ctx_n > p.max_blocks * p.bs) ctx_n = 0;  // reported when the unit runs
-        const int t1_n = min(ctx_n, nxt.z);
-        const int pe_n = min(t1_n, INT8 ? (ctx_n / p.bs) * p.bs : ctx_n);
-        const int np_n = max(0, pe_n - t0_n);
-        nt_n = (np_n + kTile - 1) / kTile;
-        blk0_n = t0_n / p.bs;
-        const int nblk_n = np_n > 0 ? min((pe_n - 1) / p.bs - blk0_n + 1, p.tab_cap) : 0;
-        float2* bsc_n = bsc_base + (tb ^ 1) * p.tab_cap;
-        const int32_t* trow_n = p.block_tables + size_t(b_n) * p.max_blocks + blk0_n;
-        for (int i = tid; i < nblk_n; i += kThreads) {
-            int id = trow_n[i];
-            if (id < 0 || id >= p.num_blocks) {
-                report(p.err, kErrBlockId);
-                id = -1;
-            }
-            tab_n[i] = id;
-            if (INT8) {
-                if (id >= 0)
-                    cp_async8(smem_addr(bsc_n + i), p.scales + (size_t(id) * p.Hkv + kvh_n) * 2);
-                else
-                    bsc_n[i] = make_float2(0.f, 0.f);
-            }
+    int ev_max = kExpNone;  // this thread's blocks; loads complete while the previous kernel drains
+    if (INT8) {
+        load_scales(0, nblk_stable);
+        for (int i = tid; i < nblk_stable; i += kThreads) {
+            const int id = tab[i];
+            if (id >= 0) ev_max = max(ev_max, v_exp(__ldg(p.scales + (size_t(id) * p.Hkv + kvh) * 2 + 1)));
         }
     }
 
@@ -681,9 +661,8 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
 
     // ---- fused step update: the split holding token ctx-1 writes that token's
     // K/V row (given in k_new / v_new) and, in INT8 mode, quantizes its block if
-    // the row filled it -- before any read of that block. (Work lists do this
-    // for all of a CTA's units at kernel start.)
-    if (!SEG && p.k_new != nullptr && ctx > 0 && t0 <= ctx - 1 && ctx - 1 < t1) {
+    // the row filled it -- before any read of that block.
+    if (p.k_new != nullptr && ctx > 0 && t0 <= ctx - 1 && ctx - 1 < t1) {
         const int bl = (ctx - 1) / p.bs - blk0;
         step_update<D, INT8>(p, b, kvh, ctx, (bl >= 0 && bl < nblk) ? tab[bl] : -1);
     }
@@ -691,41 +670,71 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
     if (lane == 0)
         for (int s = 0; s < STAGES; ++s) {
             const int tile = warp + s * kWarps;
-            if (tile >= nt_stable && tile < nt) issue(tile, (kb0 + s) % STAGES);
+            if (tile >= nt_stable && tile < nt) issue(tile, s);
         }
-    if (INT8) load_scales(nblk_stable, nblk);
-
-    WarpState<D> st;
-    st.m[0] = st.m[1] = -1e30f;
-    st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-    for (int m = 0; m < D / 16; ++m) st.acc[m][0] = st.acc[m][1] = st.acc[m][2] = st.acc[m][3] = 0.f;
-
-    // ---- INT8: the partly filled last block, read from the bf16 tail -----------
-    // Done before the pool tiles: its global loads then overlap the ring's
-    // first bulk copies instead of following the last one. Tail tile tt goes to
-    // warp kWarps-1-tt, the warps with the fewest pool tiles.
     if (INT8) {
-        const int tail_lo = max(t0, nfull);
-        const int ntail = t1 - tail_lo;
-        if (ntail > 0) {
-            const int slot = p.slots ? p.slots[b] : -1;
-            if (slot < 0 || slot >= p.max_slots) {
-                if (tid == 0) report(p.err, kErrSlot);
-            } else {
-                uint32_t qb[D / 16][2];
-                (void)q_frags<D, false>(qw, qb);
-                const float hb[2] = {p.qscale, p.qscale};
-                const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull);
-                const uint8_t* kt = static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2;
-                const uint8_t* vt = static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2;
-                for (int tt = kWarps - 1 - warp; tt * kTile < ntail; tt += kWarps) {
-                    const GmemRows kr{kt + size_t(tt) * kTile * D * 2, D * 2};
-                    const GmemRows vr{vt + size_t(tt) * kTile * D * 2, D * 2};
-                    mma_tile<D, false>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, qb, hb, g, t, st);
+        load_scales(nblk_stable, nblk);
+        // the block this step may have filled: its scale was written above
+        for (int i = nblk_stable + tid; i < nblk; i += kThreads) {
+            const int id = tab[i];
+            if (id >= 0) ev_max = max(ev_max, v_exp(__ldcg(p.scales + (size_t(id) * p.Hkv + kvh) * 2 + 1)));
+        }
+    }
+
+    // a warp's state -> o [G][D] and (m, l) [G][2] in shared memory, in plain
+    // units (acc and l times `units`); l is summed over the lanes of a head first
+    auto store_state = [&](WarpState<D>& w, float* o, float* ml, float units) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            w.l[0] += __shfl_xor_sync(kFull, w.l[0], off);
+            w.l[1] += __shfl_xor_sync(kFull, w.l[1], off);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int h = 2 * t + jj;
+            if (h < G) {
+                float* dst = o + h * D + g * (D / 8);
+#pragma unroll
+                for (int m = 0; m < D / 16; ++m) {
+                    dst[2 * m] = w.acc[m][jj] * units;
+                    dst[2 * m + 1] = w.acc[m][2 + jj] * units;
+                }
+                if (g == 0) {
+                    ml[h * 2] = w.m[jj];
+                    ml[h * 2 + 1] = w.l[jj] * units;
                 }
             }
         }
+    };
+    auto init_state = [&](WarpState<D>& w) {
+        w.m[0] = w.m[1] = w.md[0] = w.md[1] = -1e30f;
+        w.l[0] = w.l[1] = 0.f;
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) w.acc[m][0] = w.acc[m][1] = w.acc[m][2] = w.acc[m][3] = 0.f;
+    };
+
+    // ---- INT8: the partly filled last block, read from the slot's bf16 tail.
+    // Done before the pool tiles, so that its global loads overlap the ring's
+    // first bulk copies; tail tile tt goes to warp kWarps-1-tt (the warps with
+    // the fewest pool tiles), accumulated in plain units (converted to the
+    // CTA's units once those are known).
+    const int tail_lo = INT8 ? max(t0, nfull) : 0;
+    const int ntail = INT8 ? t1 - tail_lo : 0;
+    const bool tail_ok = ntail > 0 && slot >= 0 && slot < p.max_slots;
+    if (INT8 && ntail > 0 && !tail_ok && tid == 0) report(p.err, kErrSlot);
+    const int ntt = tail_ok ? (ntail + kTile - 1) / kTile : 0;  // tail tiles (<= bs / 16 <= kWarps)
+    WarpState<D> st;
+    init_state(st);
+    const bool tail_warp = INT8 && kWarps - 1 - warp < ntt;
+    if (tail_warp) {
+        const int tt = kWarps - 1 - warp;
+        uint32_t qb[D / 16][2];
+        (void)q_frags<D, false>(qw, qb);
+        const float hb[2] = {p.qscale, p.qscale};
+        const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull) + tt * kTile;
+        const GmemRows kr{static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2, D * 2};
+        const GmemRows vr{static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2, D * 2};
+        mma_tile<D, false, INT8>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, 0.f, qb, hb, g, t, st);
     }
 
     uint32_t qf[D / 16][2];
@@ -736,15 +745,43 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
         const int eh = __shfl_sync(kFull, qe, ((2 * t + jj) & 7) * 4);
         hs[jj] = p.qscale * ldexpf(1.0f, -eh);
     }
-    if (INT8) cp_async_wait_all();  // this thread's scale copies
+    if (INT8) {
+        cp_async_wait_all();  // this thread's scale copies
+        // reduced after the tail, whose loads overlap the scales' latency
+        ev_max = __reduce_max_sync(kFull, ev_max);
+        if (lane == 0) s_ev[warp] = ev_max;
+    }
     __syncthreads();
+
+    // INT8: the CTA's accumulator units (see kExpNone)
+    int ew = 14;
+    if (INT8) {
+        int e = kExpNone;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) e = max(e, s_ev[w]);
+        if (e != kExpNone) ew = e;  // else: no pool block
+    }
+    const float delta = float(14 - ew);
+    if (INT8) {
+        st.md[0] = st.m[0] - delta;
+        st.md[1] = st.m[1] - delta;
+        if (tail_warp && ew != 14) {  // the tail's plain units -> the CTA's
+            const float f = exp2i(14 - ew);
+            st.l[0] *= f;
+            st.l[1] *= f;
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) st.acc[m][i] *= f;
+        }
+    }
 
     // ---- main loop over this warp's pool tiles ----------------------------------
     int k = 0;
     bool timed_out = false;
     for (int tile = warp; tile < nt; tile += kWarps, ++k) {
-        const int s = (kb0 + k) % STAGES;
-        if (!wait_phase(bar_of(s), uint32_t((kb0 + k) / STAGES) & 1u)) {
+        const int s = k % STAGES;
+        if (!wait_phase(bar_of(s), uint32_t(k / STAGES) & 1u)) {
             timed_out = true;
             break;
         }
@@ -752,14 +789,14 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
         const int bl = tok / p.bs - blk0;
         int nvalid = min(kTile, pool_end - tok);
         if (tab[bl] < 0) nvalid = 0;
-        float ksc = 1.f, vsc = 1.f;
+        float ksc = 1.f, vmul = 1.f;
         if (INT8) {
             const float2 sc = bsc[bl];
             ksc = sc.x;
-            vsc = sc.y;
+            vmul = sc.y;
         }
         const SmemRows kr{stage_of(s), Gm::kRow}, vr{stage_of(s) + T::kTileBytes, Gm::kRow};
-        mma_tile<D, INT8>(kr, vr, nvalid, ksc, vsc, qf, hs, g, t, st);
+        mma_tile<D, INT8, INT8>(kr, vr, nvalid, ksc, vmul, delta, qf, hs, g, t, st);
         __syncwarp();
         const int nxt = tile + STAGES * kWarps;
         if (lane == 0 && nxt < nt) {
@@ -772,43 +809,10 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
         // so that no copy lands in shared memory after the CTA has exited.
         if (lane == 0) report(p.err, kErrTimeout);
         for (int kk = k; kk < k + STAGES && warp + kk * kWarps < nt; ++kk)
-            (void)wait_phase(bar_of((kb0 + kk) % STAGES), uint32_t((kb0 + kk) / STAGES) & 1u);
+            (void)wait_phase(bar_of(kk % STAGES), uint32_t(kk / STAGES) & 1u);
     }
-    const int kbn = kb0 + k;
-    // SEG: this warp's ring is empty -- start the next unit's first tiles now,
-    // so that they stream during this unit's merge and epilogue (its table was
-    // written before the barrier ahead of the main loop)
-    if (SEG && nxt.x >= 0 && lane == 0) {
-        fence_proxy_async_smem();
-        for (int s = 0; s < STAGES; ++s) {
-            const int tile = warp + s * kWarps;
-            if (tile < nt_n) issue_for(tab_n, t0_n, blk0_n, kvh_n, tile, (kbn + s) % STAGES);
-        }
-    }
-    const UnitEnd done{kbn, true, SEG && nxt.x >= 0};
 
-    // ---- merge: lanes of a warp hold disjoint dims; sum l over the 8 g lanes
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        st.l[0] += __shfl_xor_sync(kFull, st.l[0], off);
-        st.l[1] += __shfl_xor_sync(kFull, st.l[1], off);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        const int h = 2 * t + jj;
-        if (h < G) {
-            float* dst = mo_of(warp) + h * D + g * (D / 8);
-#pragma unroll
-            for (int m = 0; m < D / 16; ++m) {
-                dst[2 * m] = st.acc[m][jj];
-                dst[2 * m + 1] = st.acc[m][2 + jj];
-            }
-            if (g == 0) {
-                mml_of(warp)[h * 2] = st.m[jj];
-                mml_of(warp)[h * 2 + 1] = st.l[jj];
-            }
-        }
-    }
+    store_state(st, mo_of(warp), mml_of(warp), INT8 ? exp2i(ew - 14) : 1.f);
     __syncthreads();
 
     // ---- merge the warps and write ---------------------------------------------
@@ -816,11 +820,11 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
         // no tokens: a zero row (no partials, no counter)
         for (int e = tid; e < G * D; e += kThreads)
             reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t(b) * p.Hq + kvh * G) * D + e] = __float2bfloat16_rn(0.f);
-        return done;
+        return;
     }
     // With the fused merge, a sequence whose context fits one split has
     // nothing to merge: its only split writes the output itself.
-    const int ns = SEG ? seg_ns : SPLIT ? (ctx + p.split_tokens - 1) / p.split_tokens : 1;
+    const int ns = SPLIT ? (ctx + p.split_tokens - 1) / p.split_tokens : 1;
     const bool partial = SPLIT && !(p.ws_count && ns == 1);
     for (int e = tid; e < G * D; e += kThreads) {
         const int h = e / D, dim = e % D;
@@ -855,14 +859,12 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
         __syncthreads();
         if (tid == 0) s_last = atom_add_acq_rel_gpu(cnt, 1) == ns - 1;
         __syncthreads();
-        if (!s_last) return done;
+        if (!s_last) return;
         constexpr int EPT = (G * D + kThreads - 1) / kThreads;  // output elements per thread
         constexpr int QB = EPT >= 48 ? 1 : 48 / EPT;   // splits per batch of loads
-        // [G][ns] weights, then [G] sums: in the rings, or (SEG: the rings hold
-        // the next unit's tiles) in the merge space
-        float* wsm = SEG ? mseg : reinterpret_cast<float*>(stages);
-        const bool staged = size_t(G) * ns + G <= (SEG ? size_t(kWarps) * G * (D + 2)
-                                                       : size_t(kWarps) * STAGES * T::kStageBytes / 4);
+        // [G][ns] weights, then [G] sums, in the rings
+        float* wsm = reinterpret_cast<float*>(stages);
+        const bool staged = size_t(G) * ns + G <= size_t(kWarps) * STAGES * T::kStageBytes / 4;
         // first batch of partial outputs: issued before the weights are known
         float ov[QB][EPT];
         auto load_o = [&](int q0) {
@@ -938,70 +940,6 @@ __device__ __forceinline__ UnitEnd decode_unit(const DecodeParams& p, uint8_t* s
             }
         }
         if (tid == 0) *cnt = 0;  // ready for the next call
-    }
-    return done;
-}
-
-// Grid (split, kv head, sequence): one unit per CTA.
-template <int D, int G, bool INT8, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    pdl_launch_dependents();
-    (void)decode_unit<D, G, INT8, SPLIT, false>(p, smem, blockIdx.z, blockIdx.y, blockIdx.x, 0, 0, 0, true, 0, 0,
-                                                false, make_int4(-1, 0, 0, 0));
-}
-
-// Work list: CTA c runs units seg_offsets[c] .. seg_offsets[c+1]-1 of segs,
-// each {b, t0, t1, kvh | j << 8 | ns << 20} -- a balanced cut of all the
-// step's (sequence, kv head) token ranges, one wave of CTAs (see
-// pkv_plan_segments). Units of one CTA run back to back through the same
-// ring; an out-of-range entry is skipped and reported.
-template <int D, int G, bool INT8>
-__global__ void __launch_bounds__(kThreads, kMinCtas) decode_segments_kernel(const DecodeParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    pdl_launch_dependents();
-    const int lo = p.seg_offsets[blockIdx.x], hi = p.seg_offsets[blockIdx.x + 1];
-    const int4* segs = reinterpret_cast<const int4*>(p.segs);
-    auto valid = [&](const int4 sg) {
-        const int b = sg.x, kvh = sg.w & 0xFF, j = (sg.w >> 8) & 0xFFF, ns = (sg.w >> 20) & 0xFFF;
-        return b >= 0 && b < p.B && kvh < p.Hkv && j < ns && ns <= p.max_splits && sg.y >= 0 && sg.y <= sg.z &&
-               (sg.y % kTile) == 0;
-    };
-    pdl_wait();  // the previous kernel (and so the previous layer) has completed
-    // the step updates of all this CTA's units first: every bulk copy after
-    // this point reads settled blocks, so units can prefetch one another's
-    if (p.k_new != nullptr)
-        for (int i = lo; i < hi; ++i) {
-            const int4 sg = __ldg(segs + i);
-            if (!valid(sg)) continue;
-            const int ctx = p.ctx_lens[sg.x];
-            if (ctx <= 0 || ctx > p.max_blocks * p.bs || sg.y > ctx - 1 || ctx - 1 >= sg.z) continue;
-            const int blk = (ctx - 1) / p.bs;
-            int id = p.block_tables[size_t(sg.x) * p.max_blocks + blk];
-            if (id < 0 || id >= p.num_blocks) id = -1;
-            step_update<D, INT8>(p, sg.x, sg.w & 0xFF, ctx, id);
-        }
-    int kb = 0, tb = 0;
-    bool init = true, pre = false;
-    for (int i = lo; i < hi; ++i) {
-        const int4 sg = __ldg(segs + i);
-        if (!valid(sg)) {
-            if (threadIdx.x == 0) report(p.err, kErrSegment);
-            pre = false;
-            continue;
-        }
-        int4 nx = make_int4(-1, 0, 0, 0);
-        if (i + 1 < hi) {
-            nx = __ldg(segs + i + 1);
-            if (!valid(nx)) nx.x = -1;
-        }
-        const UnitEnd e = decode_unit<D, G, INT8, true, true>(p, smem, sg.x, sg.w & 0xFF, (sg.w >> 8) & 0xFFF, sg.y,
-                                                              sg.z, (sg.w >> 20) & 0xFFF, init, kb, tb, pre, nx);
-        kb = e.kb;
-        init = init && !e.inited;
-        pre = e.preissued;
-        tb ^= 1;
-        __syncthreads();  // the next unit reuses the table buffers and the merge space
     }
 }
 

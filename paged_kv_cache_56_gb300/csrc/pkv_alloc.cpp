@@ -229,71 +229,3 @@ int pkv_build_block_tables(const pkv_allocator* a, const int64_t* req_ids, int32
 }
 
 }  // extern "C"
-
-// ---- work-list planner for decode over sequences of mixed lengths ----------
-// Every (sequence, kv head) pair is a run of ctx tokens, rounded up to the
-// granule; the runs, laid end to end sequence by sequence, are cut into
-// num_ctas pieces of (nearly) equal length. A piece is a list of units, each
-// one pair's token range; a pair cut by a piece boundary becomes several
-// splits merged by the decode kernel (the last to arrive merges). All CTAs
-// then start together and finish together: no second wave, no idle tail.
-extern "C" int pkv_plan_segments(const int32_t* ctx_lens, int32_t B, int32_t num_kv_heads, int32_t granule,
-                                 int32_t num_ctas, int32_t* seg_offsets, int32_t* segs, int32_t seg_cap,
-                                 int32_t* info) {
-    if (B < 0 || num_kv_heads <= 0 || num_kv_heads > 255 || granule <= 0 || num_ctas <= 0 || seg_cap < 0 ||
-        !seg_offsets || !info || (B > 0 && !ctx_lens) || (seg_cap > 0 && !segs))
-        return PKV_ERR_INVALID;
-    int64_t total = 0;
-    for (int32_t b = 0; b < B; ++b) {
-        if (ctx_lens[b] < 0) return PKV_ERR_INVALID;
-        total += (int64_t(ctx_lens[b]) + granule - 1) / granule * granule * num_kv_heads;
-    }
-    // piece length: a whole number of granules, at least one
-    const int64_t per = std::max<int64_t>(granule, (total / granule + num_ctas - 1) / num_ctas * granule);
-    int32_t n = 0, cta = 0, max_ns = 1, max_len = 0;
-    int64_t room = per;
-    seg_offsets[0] = 0;
-    auto emit = [&](int32_t b, int32_t h, int32_t t0, int32_t t1) -> bool {
-        if (n >= seg_cap) return false;
-        int32_t* e = segs + size_t(n) * 4;
-        e[0] = b;
-        e[1] = t0;
-        e[2] = t1;
-        e[3] = h;  // split index and count are filled in below
-        ++n;
-        return true;
-    };
-    for (int32_t b = 0; b < B; ++b) {
-        const int32_t ctx = ctx_lens[b];
-        const int64_t run = (int64_t(ctx) + granule - 1) / granule * granule;
-        for (int32_t h = 0; h < num_kv_heads; ++h) {
-            const int32_t first = n;
-            if (run == 0) {
-                if (!emit(b, h, 0, 0)) return PKV_ERR_TOO_LARGE;  // writes the zero row
-            }
-            for (int64_t pos = 0; pos < run;) {
-                if (room == 0) {
-                    seg_offsets[++cta] = n;
-                    room = per;
-                }
-                const int64_t take = std::min(room, run - pos);
-                const int32_t t0 = int32_t(pos), t1 = int32_t(std::min<int64_t>(pos + take, ctx));
-                if (!emit(b, h, t0, t1)) return PKV_ERR_TOO_LARGE;
-                max_len = std::max(max_len, t1 - t0);
-                pos += take;
-                room -= take;
-            }
-            const int32_t ns = n - first;
-            if (ns > 4095) return PKV_ERR_TOO_LARGE;
-            max_ns = std::max(max_ns, ns);
-            for (int32_t i = first; i < n; ++i) segs[size_t(i) * 4 + 3] |= ((i - first) << 8) | (ns << 20);
-        }
-    }
-    const int32_t used = n > 0 ? cta + 1 : 0;
-    for (int32_t c = cta + 1; c <= num_ctas; ++c) seg_offsets[c] = n;
-    info[0] = n;
-    info[1] = max_ns;
-    info[2] = max_len;
-    info[3] = used;
-    return PKV_OK;
-}

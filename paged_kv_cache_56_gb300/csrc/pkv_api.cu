@@ -7,11 +7,14 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdint>
 #include <utility>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pkv.h"
-#include "kernels.cuh"
+#include "decode_registry.h"
 
 namespace pkv {
 
@@ -192,54 +195,18 @@ static int launch(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
-using DecodeFn = void (*)(DecodeParams);
-
-template <int D, bool INT8, bool SPLIT>
-static DecodeFn pick_g(int g) {
-    switch (g) {
-        case 1: return decode_kernel<D, 1, INT8, SPLIT>;
-        case 2: return decode_kernel<D, 2, INT8, SPLIT>;
-        case 4: return decode_kernel<D, 4, INT8, SPLIT>;
-        case 8: return decode_kernel<D, 8, INT8, SPLIT>;
-        default: return nullptr;
-    }
-}
-
-template <int D, bool INT8>
-static DecodeFn pick_seg_g(int g) {
-    switch (g) {
-        case 1: return decode_segments_kernel<D, 1, INT8>;
-        case 2: return decode_segments_kernel<D, 2, INT8>;
-        case 4: return decode_segments_kernel<D, 4, INT8>;
-        case 8: return decode_segments_kernel<D, 8, INT8>;
-        default: return nullptr;
-    }
-}
-
-// The work-list decode instantiation for a shape (state indices 32..47).
-static DecodeFn pick_segments(int d, int g, bool int8, int* index) {
-    const int lg = g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3;
-    *index = 32 + ((d == 128) * 4 + lg) * 2 + int8;
-    if (d == 128) return int8 ? pick_seg_g<128, true>(g) : pick_seg_g<128, false>(g);
-    return int8 ? pick_seg_g<64, true>(g) : pick_seg_g<64, false>(g);
-}
-
 // The decode instantiation for a shape, and a small index for per-kernel state.
-static DecodeFn pick_decode(int d, int g, bool int8, bool split, int* index) {
+static DecodeFn pick_decode(int d, int g, bool int8, bool split, bool hook, int* index) {
     const int lg = g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3;
-    *index = (((d == 128) * 4 + lg) * 2 + int8) * 2 + split;
-    if (d == 128) {
-        if (int8) return split ? pick_g<128, true, true>(g) : pick_g<128, true, false>(g);
-        return split ? pick_g<128, false, true>(g) : pick_g<128, false, false>(g);
-    }
-    if (int8) return split ? pick_g<64, true, true>(g) : pick_g<64, true, false>(g);
-    return split ? pick_g<64, false, true>(g) : pick_g<64, false, false>(g);
+    *index = ((((d == 128) * 4 + lg) * 2 + int8) * 2 + split) * 2 + hook;
+    if (d == 128) return int8 ? decode_fn_d128_int8(g, split, hook) : decode_fn_d128_bf16(g, split, hook);
+    return int8 ? decode_fn_d64_int8(g, split, hook) : decode_fn_d64_bf16(g, split, hook);
 }
 
 // Raises the kernel's dynamic shared-memory limit (once per kernel, device
 // and size) so that it can be launched or sized with `smem` bytes.
 static int allow_smem(DecodeFn fn, int index, size_t smem) {
-    static int configured[48][64] = {};
+    static int configured[64][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (int(smem) > configured[index][dev]) {
@@ -257,20 +224,13 @@ static int allow_smem(DecodeFn fn, int index, size_t smem) {
     return PKV_OK;
 }
 
+// Dynamic shared memory of a decode CTA: rings and mbarriers, the block table
+// (tab_cap entries) and, INT8, the block scales.
 static size_t decode_smem(int d, bool int8, int tab_cap) {
     size_t fixed = 0;
     if (d == 64) fixed = int8 ? decode_smem_fixed<64, true>() : decode_smem_fixed<64, false>();
     else fixed = int8 ? decode_smem_fixed<128, true>() : decode_smem_fixed<128, false>();
     return fixed + size_t(tab_cap) * (int8 ? 12 : 4);
-}
-
-// Work-list CTAs: two tables and two scale buffers (this unit's and the
-// next one's) and a merge space of their own ([warps][G][d] + [warps][G][2]).
-static size_t decode_smem_seg(int d, int g, bool int8, int tab_cap) {
-    size_t fixed = 0;
-    if (d == 64) fixed = int8 ? decode_smem_fixed<64, true>() : decode_smem_fixed<64, false>();
-    else fixed = int8 ? decode_smem_fixed<128, true>() : decode_smem_fixed<128, false>();
-    return fixed + size_t(tab_cap) * 2 * (4 + 8) + size_t(kWarps) * g * (size_t(d) + 2) * 4;
 }
 
 }  // namespace pkv
@@ -431,7 +391,7 @@ int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_
     const size_t smem = decode_smem(c->head_dim, int8, decode_tab_cap(c, split_tokens, max_blocks));
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
     int index = 0;
-    DecodeFn fn = pick_decode(c->head_dim, g, int8, split_tokens > 0, &index);
+    DecodeFn fn = pick_decode(c->head_dim, g, int8, split_tokens > 0, false, &index);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
     int n = 0;
@@ -442,7 +402,7 @@ int pkv_decode_ctas_per_sm(const pkv_cache_desc* c, int32_t split_tokens, int32_
 static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
                        const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                        int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits, float* ws_o, float* ws_ml,
-                       int32_t* ws_count, void* out, void* stream, const pkv_segment_plan* plan = nullptr) {
+                       int32_t* ws_count, void* out, void* stream) {
     int st = check_desc(c);
     if (st != PKV_OK) return st;
     if (B < 0 || max_blocks <= 0 || split_tokens < 0 || !(sm_scale == sm_scale)) return PKV_ERR_INVALID;
@@ -453,28 +413,16 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     if (int8 && !slots) return PKV_ERR_INVALID;
     const int64_t max_ctx = int64_t(max_blocks) * c->block_size;
     if (max_ctx > 0x7FFFFFFF) return PKV_ERR_INVALID;
-    if (plan) {  // work-list mode: the plan replaces the uniform split
-        if (!plan->seg_offsets || !plan->segs || !aligned16(plan->segs) || plan->num_ctas <= 0 ||
-            plan->max_splits <= 0 || plan->max_splits > 4095 || plan->max_unit_tokens < 0 || !ws_count)
-            return PKV_ERR_INVALID;
-        split_tokens = 0;
-        max_splits = plan->max_splits;
-        if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
-    }
-    const bool split = split_tokens > 0 || plan;
-    if (split && !plan) {
+    const bool split = split_tokens > 0;
+    if (split) {
         if (split_tokens % c->block_size || split_tokens % kTile) return PKV_ERR_INVALID;
         if (int64_t(max_splits) * split_tokens < max_ctx || max_splits > 65535) return PKV_ERR_INVALID;
         if (!ws_o || !ws_ml || !aligned16(ws_o) || !aligned16(ws_ml)) return PKV_ERR_INVALID;
+        if (ws_count && (reinterpret_cast<uintptr_t>(ws_count) & 3u)) return PKV_ERR_INVALID;
     }
-    if (split && ws_count && (reinterpret_cast<uintptr_t>(ws_count) & 3u)) return PKV_ERR_INVALID;
     const int g = c->num_q_heads / c->num_kv_heads;
-    int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
-    if (plan) {
-        tab_cap = std::min<int64_t>(max_blocks, int64_t(plan->max_unit_tokens) / c->block_size + 2);
-        tab_cap += tab_cap & 1;
-    }
-    const size_t smem = plan ? decode_smem_seg(c->head_dim, g, int8, tab_cap) : decode_smem(c->head_dim, int8, tab_cap);
+    const int tab_cap = decode_tab_cap(c, split_tokens, max_blocks);
+    const size_t smem = decode_smem(c->head_dim, int8, tab_cap);
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
     DecodeParams p;
@@ -506,15 +454,11 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     p.tab_cap = tab_cap;
     p.qscale = sm_scale * 1.4426950408889634f;
     p.skip_copy = g_skip_copy.load(std::memory_order_relaxed);
-    p.seg_offsets = plan ? plan->seg_offsets : nullptr;
-    p.segs = plan ? plan->segs : nullptr;
-    p.B = B;
 
-    const dim3 grid = plan ? dim3(unsigned(plan->num_ctas), 1u, 1u)
-                           : dim3(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
+    const dim3 grid(split ? unsigned(max_splits) : 1u, unsigned(c->num_kv_heads), unsigned(B));
     auto s = static_cast<cudaStream_t>(stream);
     int index = 0;
-    DecodeFn fn = plan ? pick_segments(c->head_dim, g, int8, &index) : pick_decode(c->head_dim, g, int8, split, &index);
+    DecodeFn fn = pick_decode(c->head_dim, g, int8, split, p.skip_copy >= 0, &index);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if ((st = allow_smem(fn, index, smem)) != PKV_OK) return st;
     if ((st = launch(fn, grid, dim3(kThreads), smem, s, p)) != PKV_OK) return st;
@@ -545,36 +489,40 @@ int pkv_decode_layers(const pkv_cache_desc* descs, int32_t num_layers, const voi
     const auto* vb = static_cast<const uint8_t*>(v_new);
     auto* ob = static_cast<uint8_t*>(out);
     for (int32_t l = 0; l < num_layers; ++l) {
+        // one NVTX range per layer (visible to a profiler attached to the process)
+        char name[32];
+        snprintf(name, sizeof(name), "pkv layer %d", int(l));
+        nvtxRangePushA(name);
         const int rc = decode_impl(descs + l, qb + l * q_layer_stride, kb ? kb + l * kv_layer_stride : nullptr,
                                    vb ? vb + l * kv_layer_stride : nullptr, block_tables, max_blocks, ctx_lens, slots,
                                    B, sm_scale, split_tokens, max_splits, ws_o, ws_ml, ws_count,
                                    ob + l * out_layer_stride, stream);
+        nvtxRangePop();
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;
 }
 
-int pkv_decode_layers_planned(const pkv_cache_desc* descs, int32_t num_layers, const void* q,
-                              int64_t q_layer_stride, const void* k_new, const void* v_new, int64_t kv_layer_stride,
-                              void* out, int64_t out_layer_stride, const int32_t* block_tables, int32_t max_blocks,
-                              const int32_t* ctx_lens, const int32_t* slots, int32_t B, float sm_scale,
-                              const pkv_segment_plan* plan, float* ws_o, float* ws_ml, int32_t* ws_count,
-                              void* stream) {
-    if (!descs || num_layers < 0 || !q || !out || !plan) return PKV_ERR_INVALID;
-    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
-    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
-    if ((q_layer_stride | out_layer_stride | (k_new ? kv_layer_stride : 0)) & 15) return PKV_ERR_INVALID;
-    const auto* qb = static_cast<const uint8_t*>(q);
-    const auto* kb = static_cast<const uint8_t*>(k_new);
-    const auto* vb = static_cast<const uint8_t*>(v_new);
-    auto* ob = static_cast<uint8_t*>(out);
-    for (int32_t l = 0; l < num_layers; ++l) {
-        const int rc = decode_impl(descs + l, qb + l * q_layer_stride, kb ? kb + l * kv_layer_stride : nullptr,
-                                   vb ? vb + l * kv_layer_stride : nullptr, block_tables, max_blocks, ctx_lens, slots,
-                                   B, sm_scale, 0, 0, ws_o, ws_ml, ws_count, ob + l * out_layer_stride, stream, plan);
-        if (rc != PKV_OK) return rc;
+int pkv_sync_status(const pkv_cache_desc* descs, int32_t n, void* stream, int32_t* out_bits) {
+    if (out_bits) *out_bits = 0;
+    if (n < 0 || (n > 0 && !descs)) return PKV_ERR_INVALID;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    int32_t bits = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t* w = descs[i].err_word;
+        if (!w) continue;
+        int32_t v = 0;
+        if (cudaMemcpyAsync(&v, w, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (v && cudaMemsetAsync(w, 0, sizeof(v), s) != cudaSuccess) return PKV_ERR_CUDA;
+        bits |= v;
     }
-    return PKV_OK;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (out_bits) *out_bits = bits;
+    if (bits & PKV_DEVERR_TIMEOUT) return PKV_ERR_DEVICE_TIMEOUT;
+    return bits ? PKV_ERR_INVALID : PKV_OK;
 }
 
 int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, const void* v_new,
@@ -627,7 +575,8 @@ extern "C" int pkv_decode_attention_static_ws(const pkv_cache_desc* c, const voi
                                               int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                                               int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
                                               void* out, void* stream) {
-    if (split_tokens <= 0)  // no split: no scratch is used at all
+    if (split_tokens < 0) return PKV_ERR_INVALID;
+    if (split_tokens == 0)  // no split: no scratch is used at all
         return pkv_decode_attention(c, q, block_tables, max_blocks, ctx_lens, slots, B, sm_scale, 0, 0, nullptr,
                                     nullptr, nullptr, out, stream);
     int st = check_desc(c);

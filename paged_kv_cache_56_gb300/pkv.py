@@ -26,7 +26,8 @@ PKV_ERR_NOT_FOUND = -3
 PKV_ERR_EXISTS = -4
 PKV_ERR_UNSUPPORTED = -5
 PKV_ERR_CUDA = -6
-PKV_ERR_TOO_LARGE = -7
+PKV_ERR_DEVICE_TIMEOUT = -7
+PKV_ERR_TOO_LARGE = -8
 PKV_STATIC_WS_BYTES = 8 << 20
 
 PKV_DEVERR_BLOCK_ID = 1
@@ -41,7 +42,7 @@ PKV_DTYPE_INT8 = 1
 _NAMES = {PKV_ERR_INVALID: "PKV_ERR_INVALID", PKV_ERR_OOM: "PKV_ERR_OOM",
           PKV_ERR_NOT_FOUND: "PKV_ERR_NOT_FOUND", PKV_ERR_EXISTS: "PKV_ERR_EXISTS",
           PKV_ERR_UNSUPPORTED: "PKV_ERR_UNSUPPORTED", PKV_ERR_CUDA: "PKV_ERR_CUDA",
-          PKV_ERR_TOO_LARGE: "PKV_ERR_TOO_LARGE"}
+          PKV_ERR_DEVICE_TIMEOUT: "PKV_ERR_DEVICE_TIMEOUT", PKV_ERR_TOO_LARGE: "PKV_ERR_TOO_LARGE"}
 
 EXPORTED = (
     "pkv_allocator_create", "pkv_allocator_destroy", "pkv_alloc", "pkv_append_block", "pkv_free",
@@ -51,7 +52,7 @@ EXPORTED = (
     "pkv_splitk_ws_o_bytes", "pkv_splitk_ws_ml_bytes", "pkv_decode_ctas_per_sm",
     "pkv_decode_attention_static_ws", "pkv_set_programmatic_launch", "pkv_decode_step", "pkv_decode_layers",
     "pkv_fork", "pkv_cow_block", "pkv_block_refs", "pkv_copy_blocks", "pkv_copy_slots",
-    "pkv_plan_segments", "pkv_decode_layers_planned", "pkv_debug_skip_copy",
+    "pkv_debug_skip_copy", "pkv_sync_status",
 )
 
 
@@ -59,12 +60,6 @@ class PkvError(RuntimeError):
     def __init__(self, fn: str, code: int):
         super().__init__(f"{fn} returned {_NAMES.get(code, code)}")
         self.code = code
-
-
-class SegmentPlan(ctypes.Structure):
-    """Mirror of ``pkv_segment_plan`` (device pointers)."""
-    _fields_ = [("seg_offsets", ctypes.c_void_p), ("segs", ctypes.c_void_p), ("num_ctas", ctypes.c_int32),
-                ("max_splits", ctypes.c_int32), ("max_unit_tokens", ctypes.c_int32)]
 
 
 class CacheDesc(ctypes.Structure):
@@ -106,10 +101,7 @@ def lib() -> ctypes.CDLL:
             "pkv_block_refs": (ctypes.c_int, [_VP, _I32]),
             "pkv_copy_blocks": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP]),
             "pkv_copy_slots": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _VP, _VP, _I32, _VP]),
-            "pkv_plan_segments": (ctypes.c_int, [_I32P, _I32, _I32, _I32, _I32, _I32P, _I32P, _I32, _I32P]),
-            "pkv_decode_layers_planned": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _VP, _I64, _VP, _VP, _I64,
-                                                         _VP, _I64, _VP, _I32, _VP, _VP, _I32, ctypes.c_float,
-                                                         ctypes.POINTER(SegmentPlan), _VP, _VP, _VP, _VP]),
+            "pkv_sync_status": (ctypes.c_int, [ctypes.POINTER(CacheDesc), _I32, _VP, _I32P]),
             "pkv_num_free": (ctypes.c_int, [_VP]),
             "pkv_request_table": (ctypes.c_int, [_VP, _I64, _I32P, _I32]),
             "pkv_free_list": (ctypes.c_int, [_VP, _I32P, _I32]),
@@ -490,53 +482,19 @@ def pkv_decode_attention_static_ws(desc: CacheDesc, q: torch.Tensor, block_table
                                                 split_tokens, max_splits, outp, _stream(stream)))
 
 
-def pkv_plan_segments(ctx_lens, num_kv_heads: int, granule: int, num_ctas: int, seg_cap: int,
-                      seg_offsets: np.ndarray | None = None, segs: np.ndarray | None = None):
-    """Host work list for pkv_decode_layers_planned: (seg_offsets [num_ctas+1],
-    segs [units, 4], info {units, max_splits, max_unit_tokens, ctas_used}).
-    seg_offsets / segs may be given (int32, e.g. pinned tensors' numpy views)."""
-    ctx = _host_i32(ctx_lens)
-    if seg_offsets is None:
-        seg_offsets = np.empty(num_ctas + 1, np.int32)
-    if segs is None:
-        segs = np.empty((seg_cap, 4), np.int32)
-    if seg_offsets.size < num_ctas + 1 or segs.size < 4 * seg_cap:
-        raise ValueError("output arrays too small")
-    info = np.zeros(4, np.int32)
-    _check("pkv_plan_segments",
-           lib().pkv_plan_segments(ctx.ctypes.data_as(_I32P), ctx.size, num_kv_heads, granule, num_ctas,
-                                   seg_offsets.ctypes.data_as(_I32P), segs.ctypes.data_as(_I32P), seg_cap,
-                                   info.ctypes.data_as(_I32P)))
-    return seg_offsets, segs, dict(units=int(info[0]), max_splits=int(info[1]), max_unit_tokens=int(info[2]),
-                                   ctas_used=int(info[3]))
-
-
-def pkv_decode_layers_planned(descs: ctypes.Array, q: torch.Tensor, k_new, v_new, block_tables: torch.Tensor,
-                              ctx_lens: torch.Tensor, slots, sm_scale: float, out: torch.Tensor,
-                              plan: SegmentPlan, ws_o, ws_ml, ws_count, stream=None) -> None:
-    """pkv_decode_layers over a work list (plan: device seg_offsets / segs)."""
-    L = len(descs)
-    B = ctx_lens.numel()
-    d0 = descs[0]
-    hq, hkv, d = d0.num_q_heads, d0.num_kv_heads, d0.head_dim
-    qp = _layered(q, "q", L, (B, hq, d))
-    outp = _layered(out, "out", L, (B, hq, d))
-    kp = vp = None
-    kv_stride = 0
-    if k_new is not None:
-        if v_new is None or v_new.stride(0) != k_new.stride(0):
-            raise ValueError("k_new and v_new must be given together, with the same layer stride")
-        kp = _layered(k_new, "k_new", L, (B, hkv, d))
-        vp = _layered(v_new, "v_new", L, (B, hkv, d))
-        kv_stride = k_new.stride(0) * 2
-    max_blocks = block_tables.shape[-1] if block_tables.dim() == 2 else 0
-    tp = _dev(block_tables, "block_tables", torch.int32, B * max_blocks)
-    cp = _dev(ctx_lens, "ctx_lens", torch.int32, B)
-    sp = _opt_dev(slots, "slots", torch.int32, B)
-    wo = _dev(ws_o, "ws_o", torch.float32, B * hq * plan.max_splits * d)
-    wml = _dev(ws_ml, "ws_ml", torch.float32, B * hq * plan.max_splits * 2)
-    wc = _dev(ws_count, "ws_count", torch.int32, B * hkv)
-    _check("pkv_decode_layers_planned",
-           lib().pkv_decode_layers_planned(descs, L, qp, q.stride(0) * 2, kp, vp, kv_stride, outp,
-                                           out.stride(0) * 2, tp, max_blocks, cp, sp, B, float(sm_scale),
-                                           ctypes.byref(plan), wo, wml, wc, _stream(stream)))
+def pkv_sync_status(descs, stream=None, raise_on_error: bool = True) -> int:
+    """Waits for ``stream``, reads and clears the error words of ``descs`` (one
+    CacheDesc or a sequence of them) and returns the OR of their PKV_DEVERR_*
+    bits. With raise_on_error, a nonzero status (PKV_ERR_DEVICE_TIMEOUT for an
+    expired bounded wait, PKV_ERR_INVALID for an out-of-range value in device
+    memory) raises PkvError after the words have been cleared."""
+    if isinstance(descs, CacheDesc):
+        descs = [descs]
+    arr = descs if isinstance(descs, ctypes.Array) else desc_array(list(descs))
+    bits = ctypes.c_int32(0)
+    rc = lib().pkv_sync_status(arr, len(arr), _stream(stream), ctypes.byref(bits))
+    if raise_on_error:
+        _check("pkv_sync_status", rc)
+    elif rc not in (PKV_OK, PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_INVALID):
+        _check("pkv_sync_status", rc)
+    return bits.value

@@ -325,31 +325,13 @@ class StepBuffers:
     """Device-side control arrays (and split-K workspace) of decode steps for
     up to max_batch sequences; pinned host mirrors make the uploads async."""
 
-    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int = 0, fused_merge: bool = True,
-                 work_list_ctas: int = 0):
-        """work_list_ctas > 0: also plan each step as a work list of that many
-        CTAs (pkv_plan_segments) for pkv_decode_layers_planned; the workspace is
-        then sized for the most splits a pair can get under any plan."""
+    def __init__(self, cache: PagedKVCache, max_batch: int, split_tokens: int = 0, fused_merge: bool = True):
         dev = cache.device
         self.cache = cache
         self.max_batch = max_batch
         self.split_tokens = split_tokens
         mb = cache.max_blocks
         self.max_splits = -(-(mb * cache.bs) // split_tokens) if split_tokens else 0
-        self.ctas = work_list_ctas
-        if work_list_ctas:
-            # a pair's run is at most total / Hkv tokens and a piece at least
-            # total / ctas, so a pair meets at most ctas / Hkv + 2 pieces
-            self.max_splits = max(self.max_splits, work_list_ctas // cache.hkv + 2)
-            self.granule = max(cache.bs, 16)
-            self.seg_cap = max_batch * cache.hkv + work_list_ctas + 1
-            self.h_segoff = torch.zeros(work_list_ctas + 1, dtype=torch.int32).pin_memory()
-            self.segoff = torch.zeros(work_list_ctas + 1, dtype=torch.int32, device=dev)
-            self.h_segs = torch.zeros((self.seg_cap, 4), dtype=torch.int32).pin_memory()
-            self.segs = torch.zeros((self.seg_cap, 4), dtype=torch.int32, device=dev)
-            self.plan_info = None
-            split_tokens = split_tokens or 1  # a workspace is needed
-
         def pair(shape):
             return (torch.zeros(shape, dtype=torch.int32).pin_memory(),
                     torch.zeros(shape, dtype=torch.int32, device=dev))
@@ -387,16 +369,6 @@ class StepBuffers:
             d[:B].copy_(h[:B], non_blocking=True)
         self.h_tab[:B].numpy()[:] = plan.tables
         self.tab[:B].copy_(self.h_tab[:B], non_blocking=True)
-        if self.ctas:
-            _, _, info = pkv.pkv_plan_segments(plan.ctx_lens, self.cache.hkv, self.granule, self.ctas, self.seg_cap,
-                                               self.h_segoff.numpy(), self.h_segs.numpy())
-            self.segoff.copy_(self.h_segoff, non_blocking=True)
-            n = info["units"]
-            self.segs[:n].copy_(self.h_segs[:n], non_blocking=True)
-            self.plan_info = info
-            self.seg_plan = pkv.SegmentPlan(seg_offsets=self.segoff.data_ptr(), segs=self.segs.data_ptr(),
-                                            num_ctas=max(1, info["ctas_used"]), max_splits=self.max_splits,
-                                            max_unit_tokens=info["max_unit_tokens"])
         self.copied.record()
 
 

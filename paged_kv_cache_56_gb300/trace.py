@@ -31,6 +31,12 @@ from .runtime import PagedKVCache, StepBuffers, prefill, sm_scale_for
 
 PREFIX_SEQ = 10 ** 6  # synthetic sequence id of the shared prefix rows
 
+# Launch configuration of the trace's decode steps: split length in tokens
+# (measured best on GB300 among 512..4096 for this workload) and
+# programmatic dependent launch between the layers' kernels.
+TRACE_SPLIT_TOKENS = 1536
+TRACE_PDL = True
+
 
 @dataclass
 class Request:
@@ -51,7 +57,7 @@ class TraceDriver:
     def __init__(self, cache: PagedKVCache, seed: int, num_steps: int, max_running: int = 128,
                  prefix_tokens: int = 200, arrival_rate: float = 2.0, prompt_min: int = 16,
                  prompt_max: int = 4096, mean_output: float = 300.0, split_tokens: int = 0,
-                 fused: bool = True, work_list: bool = False):
+                 fused: bool = True):
         self.cache = cache
         self.seed = seed
         self.max_running = max_running
@@ -66,15 +72,7 @@ class TraceDriver:
         self.finished: list[Request] = []
         self.step_no = 0
         self._next_arrival = 0
-        # work_list: each step's (sequence, kv head) token runs are cut into one
-        # wave of equal pieces (pkv_plan_segments) instead of a uniform split
-        self.work_list = work_list
-        ctas = 0
-        if work_list:
-            sms = torch.cuda.get_device_properties(cache.device).multi_processor_count
-            ctas = sms * pkv.pkv_decode_ctas_per_sm(cache.layers[0].desc, max(split_tokens, cache.bs),
-                                                    cache.max_blocks)
-        self.bufs = StepBuffers(cache, max_running, split_tokens, fused_merge=True, work_list_ctas=ctas)
+        self.bufs = StepBuffers(cache, max_running, split_tokens, fused_merge=True)
         self.out = torch.empty((cache.L, max_running, cache.hq, cache.d), dtype=torch.bfloat16,
                                device=cache.device)
         self.prefix_ids = []
@@ -176,13 +174,8 @@ class TraceDriver:
             vs = torch.stack([x[2] for x in inputs])
             if events is not None:
                 events[0].record()
-            if self.work_list:
-                pkv.pkv_decode_layers_planned(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B],
-                                              self.sm_scale, self.out[:, :B], b.seg_plan, b.ws_o, b.ws_ml,
-                                              b.ws_count)
-            else:
-                pkv.pkv_decode_layers(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
-                                      self.out[:, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
+            pkv.pkv_decode_layers(self.descs, qs, ks, vs, b.tab[:B], b.ctx[:B], b.slot[:B], self.sm_scale,
+                                  self.out[:, :B], b.split_tokens, b.max_splits, b.ws_o, b.ws_ml, b.ws_count)
             if events is not None:
                 events[1].record()
             c.commit_step(rids)

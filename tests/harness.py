@@ -40,11 +40,16 @@ class Workload:
                  num_blocks: int, int8, split_tokens: int = 0, max_blocks: int | None = None,
                  head_scale: bool = False, outliers: bool = False, shuffle: bool = True,
                  req_ids=None, device="cuda", fused_merge: bool = True, graph: bool = False, repeat: int = 1,
-                 fused_step: bool | None = None):
+                 fused_step: bool | None = None, kv_scale=None):
+        """kv_scale: optional fn(layer, kind, positions) -> fp32 [T, Hkv] (CPU)
+        multiplying the generated K (kind synth.KIND_K) or V rows of tokens at
+        ``positions`` per kv head (applied in fp32, then rounded to bf16: the
+        same bits on either device)."""
         self.seed, self.L, self.prior = seed, num_layers, list(prior)
         self.Hq, self.Hkv, self.d, self.bs = Hq, Hkv, d, bs
         self.int8 = int8
         self.head_scale, self.outliers = head_scale, outliers
+        self.kv_scale = kv_scale
         self.B = len(self.prior)
         self.req_ids = list(req_ids) if req_ids is not None else list(range(100, 100 + self.B))
         self.sm_scale = 1.0 / math.sqrt(d)
@@ -88,8 +93,13 @@ class Workload:
         return synth.head_multipliers(self.seed, layer, synth.KIND_Q, self.Hq) if self.head_scale else None
 
     def kv(self, layer, kind, req, positions, device=None):
-        return synth.kv_rows(self.seed, layer, kind, req, positions, self.Hkv, self.d,
+        rows = synth.kv_rows(self.seed, layer, kind, req, positions, self.Hkv, self.d,
                              mult=self.kv_mult(layer, kind), device=device or self.device)
+        if self.kv_scale is not None:
+            pos = torch.as_tensor(positions, dtype=torch.int64).reshape(-1).cpu()
+            m = self.kv_scale(layer, kind, pos).to(torch.float32).to(rows.device)
+            rows = (rows.float() * m[:, :, None]).to(torch.bfloat16)
+        return rows
 
     def q(self, layer, step, reqs, device=None):
         return synth.q_rows(self.seed, layer, step, reqs, self.Hq, self.d, mult=self.q_mult(layer),

@@ -93,6 +93,30 @@ def test_argument_validation(L):
     assert L.pkv_splitk_reduce(16, 16, 16, 1, 4, 128, 0, 2, 16, None) == pkv.PKV_ERR_INVALID
     assert pkv.pkv_splitk_ws_o_bytes(2, 3, 128, 5) == 2 * 3 * 5 * 128 * 4
     assert pkv.pkv_splitk_ws_ml_bytes(2, 3, 5) == 2 * 3 * 5 * 2 * 4
+    # the no-allocation entry point rejects a negative split like the regular one
+    static = L.pkv_decode_attention_static_ws
+    assert static(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, -16, 2, 16, None) == pkv.PKV_ERR_INVALID
+    assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, -16, 2, 16, 16, None, 16, None) == pkv.PKV_ERR_INVALID
+    # the error-word reader: bad counts and a NULL array are refused before any CUDA call
+    bits = ctypes.c_int32(7)
+    assert L.pkv_sync_status(None, 1, None, ctypes.byref(bits)) == pkv.PKV_ERR_INVALID
+    assert L.pkv_sync_status(ctypes.byref(d), -1, None, ctypes.byref(bits)) == pkv.PKV_ERR_INVALID
+    assert bits.value == 0
+
+
+def test_status_codes_match_header():
+    """The binding's status constants are the header's, and the device-timeout
+    status has the value the boundary fixes for it (-7), distinct from every
+    other status."""
+    src = open(HEADER).read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(PKV_(?:OK|ERR_\w+))\s+(-?\d+)", src)}
+    assert codes["PKV_OK"] == 0 and codes["PKV_ERR_DEVICE_TIMEOUT"] == -7
+    assert len(set(codes.values())) == len(codes)
+    for name, value in codes.items():
+        assert getattr(pkv, name) == value, name
+    bits = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(PKV_DEVERR_\w+)\s+(\d+)", src)}
+    for name, value in bits.items():
+        assert getattr(pkv, name) == value, name
 
 
 def test_binding_refuses_host_tensors():
@@ -294,57 +318,6 @@ def test_fork_and_cow_errors(L):
         assert pkv.pkv_free_list(h) == [3, 4, 5, 1]
     finally:
         pkv.pkv_allocator_destroy(h)
-
-
-@pytest.mark.parametrize("granule", [16, 64])
-def test_plan_segments_covers_every_pair_once(L, granule):
-    """The work list cuts the (sequence, kv head) runs -- each rounded up to the
-    granule -- into num_ctas equal pieces: every pair's tokens covered once,
-    in order, cut only at granule multiples; split indices and counts
-    consistent; pieces balanced to within one granule; empty contexts get one
-    empty unit (their zero row)."""
-    rng = random.Random(granule)
-    for trial in range(200):
-        B = rng.randint(0, 40)
-        hkv = rng.choice([1, 2, 8])
-        ctas = rng.choice([1, 3, 7, 64, 608])
-        ctx = [rng.choice([0, 1, 15, 16, 17, 63, 64, 65]) if rng.random() < 0.3 else rng.randint(0, 5000)
-               for _ in range(B)]
-        cap = B * hkv + ctas + 1
-        off, segs, info = pkv.pkv_plan_segments(ctx, hkv, granule, ctas, cap)
-        n = info["units"]
-        assert off[0] == 0 and off[ctas] == n and all(off[i] <= off[i + 1] for i in range(ctas))
-        assert info["ctas_used"] <= ctas
-        runs = {}
-        piece_len = [0] * ctas
-        for c in range(ctas):
-            for i in range(off[c], off[c + 1]):
-                b, t0, t1, w = segs[i]
-                h, j, ns = w & 0xFF, (w >> 8) & 0xFFF, (w >> 20) & 0xFFF
-                runs.setdefault((b, h), []).append((t0, t1, j, ns))
-                assert t0 % granule == 0 and t0 <= t1 <= ctx[b]
-                piece_len[c] += (-(-t1 // granule) * granule if t1 == ctx[b] else t1) - t0
-        assert set(runs) == {(b, h) for b in range(B) for h in range(hkv)}
-        max_ns = 1
-        for (b, h), us in runs.items():
-            ns = len(us)
-            max_ns = max(max_ns, ns)
-            assert [u[2] for u in us] == list(range(ns)) and all(u[3] == ns for u in us)
-            if ctx[b] == 0:
-                assert us == [(0, 0, 0, 1)]
-                continue
-            assert us[0][0] == 0 and us[-1][1] == ctx[b]
-            assert all(us[k][1] == us[k + 1][0] for k in range(ns - 1))
-        assert info["max_splits"] == max_ns <= ctas // hkv + 2
-        total = sum(-(-c // granule) * granule for c in ctx) * hkv
-        if total:
-            per = max(granule, -(-(total // granule) // ctas) * granule)
-            used = [x for x in piece_len if x]
-            assert max(used) <= per and sum(piece_len) == total
-            assert all(x == per for x in piece_len[: info["ctas_used"] - 1])
-    with pytest.raises(pkv.PkvError) as e:
-        pkv.pkv_plan_segments([100, 200], 2, 16, 8, 3)
-    assert e.value.code == pkv.PKV_ERR_TOO_LARGE
 
 
 def test_cache_stats_count_blocks_and_tail_waste(L):

@@ -79,7 +79,11 @@ def test_bad_table_entries_are_reported_and_skipped():
     assert lc.error_bits() & pkv.PKV_DEVERR_BLOCK_ID
     # the valid block still contributes: V == 2 everywhere there
     assert torch.allclose(out.float(), torch.full_like(out.float(), 2.0))
-    lc.err.zero_()
+    # an out-of-range value in device memory reads back as PKV_ERR_INVALID
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_sync_status(lc.desc)
+    assert e.value.code == pkv.PKV_ERR_INVALID
+    assert pkv.pkv_sync_status(lc.desc, raise_on_error=False) == 0  # cleared
     ctx = torch.tensor([33], dtype=torch.int32, device="cuda")  # more than 2 blocks * 16
     pkv.pkv_decode_attention(lc.desc, q, torch.tensor([[0, 1]], dtype=torch.int32, device="cuda"), ctx, None,
                              0.125, out)
@@ -147,15 +151,18 @@ def test_bounded_wait_runs_out_and_the_gpu_recovers(split):
     from harness import Workload
     w = Workload(seed=23, num_layers=1, prior=(100, 17, 33, 1), Hq=4, Hkv=2, d=64, bs=16, num_blocks=64, int8=True,
                  split_tokens=split, max_blocks=9)
+    descs = [lc.desc for lc in w.cache.layers]
     pkv.pkv_debug_skip_copy(0)  # tile 0 of warp 0 of the first CTA: sequence 0 has pool tiles
     try:
         w.step()
-        torch.cuda.synchronize()
+        # the status call waits for the step, reads the error word and clears it
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_sync_status(descs)
+        assert e.value.code == pkv.PKV_ERR_DEVICE_TIMEOUT
     finally:
         pkv.pkv_debug_skip_copy(-1)
-    assert w.error_bits() & pkv.PKV_DEVERR_TIMEOUT
-    for lc in w.cache.layers:
-        lc.err.zero_()
+    assert w.error_bits() == 0
+    assert pkv.pkv_sync_status(descs) == 0
     out = w.step().float().cpu().numpy()  # the cache itself was written by the append kernels
     for i in range(w.B):
         assert_close(out[0, i], w.oracle_out(0, i, 1), f"seq {i}")
