@@ -1,8 +1,9 @@
 """The continuous-batching trace (200 decode steps, up to 128 running
 requests, Hq=32, Hkv=8, d=128, 16-token blocks, INT8 cache, 32 layers, a
-200-token shared prefix): sampled outputs against the oracle every 20th
-step, block conservation every step, and the pools of sampled requests byte
-for byte at the end."""
+200-token shared prefix), in the launch configuration the benchmark times
+(its split length, programmatic dependent launch, longest context first):
+sampled outputs against the oracle every 20th step, block conservation every
+step, and the pools of sampled requests byte for byte at the end."""
 
 import gc
 import math
@@ -17,7 +18,7 @@ from oracle.attention import decode_attention
 from oracle.cache import SequenceHistory
 from paged_kv_cache_56_gb300 import pkv, synth
 from paged_kv_cache_56_gb300.runtime import PagedKVCache
-from paged_kv_cache_56_gb300.trace import PREFIX_SEQ, TraceDriver
+from paged_kv_cache_56_gb300.trace import PREFIX_SEQ, TRACE_PDL, TRACE_SPLIT_TOKENS, TraceDriver
 
 pytestmark = pytest.mark.gpu
 
@@ -35,12 +36,13 @@ def _history(drv: TraceDriver, layer: int, rid: int, n: int) -> SequenceHistory:
 @pytest.fixture(scope="module")
 def run():
     ensure_built()
-    pkv.pkv_set_programmatic_launch(False)
+    pkv.pkv_set_programmatic_launch(TRACE_PDL)
     max_blocks = -(-(200 + 4096 + STEPS + 16) // BS)
     cache = PagedKVCache(L, POOL, HQ, HKV, D, BS, True, max_slots=129, max_blocks_per_seq=max_blocks,
                          initial_order=synth.permutation(SEED, POOL))
-    drv = TraceDriver(cache, SEED, STEPS, max_running=128, split_tokens=512)
+    drv = TraceDriver(cache, SEED, STEPS, max_running=128, split_tokens=TRACE_SPLIT_TOKENS)
     yield drv
+    pkv.pkv_set_programmatic_launch(False)
     cache.close()
     del drv, cache
     gc.collect()
