@@ -263,16 +263,16 @@ def run_trace(args, wl):
     are inside the CUDA events (admission prefill is setup, not the path)."""
     from paged_kv_cache_56_gb300 import pkv, synth
     from paged_kv_cache_56_gb300.runtime import PagedKVCache
-    from paged_kv_cache_56_gb300.trace import TraceDriver
+    from paged_kv_cache_56_gb300.trace import TRACE_PDL, TRACE_SPLIT_TOKENS, TraceDriver
 
-    pkv.pkv_set_programmatic_launch(not args.no_pdl)
+    pkv.pkv_set_programmatic_launch(TRACE_PDL and not args.no_pdl)
     total_steps = args.warmup + args.steps
     bs = wl["bs"]
     cache = PagedKVCache(wl["L"], wl["num_blocks"], wl["Hq"], wl["Hkv"], wl["d"], bs, wl["int8"],
                          max_slots=wl["B"] + 1, max_blocks_per_seq=-(-(200 + 4096 + total_steps + 16) // bs),
                          device=f"cuda:{torch.cuda.current_device()}",
                          initial_order=synth.permutation(SEED, wl["num_blocks"]))
-    split = args.split if args.split is not None else 1536  # measured best at this workload (512..4096 swept)
+    split = args.split if args.split is not None else TRACE_SPLIT_TOKENS
     drv = TraceDriver(cache, SEED, total_steps, max_running=wl["B"], split_tokens=split)
     for _ in range(args.warmup):
         drv.step()
@@ -444,49 +444,132 @@ def run_device(args, wl, rank, world):
 # the oracle arm (CPU)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, steps: int, budget_s: float = 20.0):
-    """Times the oracle on a bounded sample of the workload: decode steps of
-    the first layer's sequences (every query head), histories prebuilt
-    (untimed), each step = append one row + the oracle's context read +
-    fp64 attention. Returns (KV GB/s, tokens/s, sample description, cores)."""
+def _oracle_contexts(wl) -> list:
+    """Context lengths the CPU sample decodes from: the workload's own, or for
+    the trace, the shared prefix plus the first requests' prompts."""
+    if wl.get("steps"):  # the trace: 200-token prefix + log-uniform prompts
+        from paged_kv_cache_56_gb300 import synth
+        return [200 + p for _, _, p, _ in synth.trace_requests(SEED, 40)[:16]]
+    return wl["prior"] if isinstance(wl["prior"], list) else [wl["prior"]] * wl["B"]
+
+
+_POOL_BARRIER = None
+
+
+def _pool_init(barrier):
+    global _POOL_BARRIER
+    _POOL_BARRIER = barrier
+
+
+def _f32(a: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact)."""
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def _oracle_task(task):
+    """One worker's share of the CPU sample. For each (sequence, kv head) unit
+    a one-head history of the context is built (untimed); then, after a
+    barrier with the other workers (sync), each step appends the unit's new
+    row and runs the oracle's context read and fp64 attention for the kv
+    head's query group. Returns (seconds in the timed region, steps done,
+    bytes, unit-steps)."""
+    meta, units, steps, budget_s, sync = task
     from oracle.attention import decode_attention
     from oracle.cache import SequenceHistory
-    from paged_kv_cache_56_gb300 import synth
+    d, bs, int8, G = meta["d"], meta["bs"], meta["int8"], meta["G"]
+    work = []
+    for n, k, v, qs in units:
+        hist = SequenceHistory(1, d, bs, int8)
+        hist.append(_f32(k[:n]), _f32(v[:n]))
+        work.append((n, hist, _f32(k[n:]), _f32(v[n:]), _f32(qs)))
+    sm = 1.0 / math.sqrt(d)
+    if sync:
+        _POOL_BARRIER.wait()
+    done_bytes = done = 0
+    t0 = time.perf_counter()
+    s = 0
+    while s < steps:
+        for n, hist, kn, vn, qs in work:
+            hist.append(kn[s:s + 1], vn[s:s + 1])
+            kc, vc = hist.context()
+            decode_attention(qs[s], kc, vc, sm)
+            done_bytes += attention_bytes([n + s + 1], G, 1, d, bs, int8)
+            done += 1
+        s += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    return time.perf_counter() - t0, s, done_bytes, done
 
-    B, Hq, Hkv, d, bs = wl["B"], wl["Hq"], wl["Hkv"], wl["d"], wl["bs"]
-    prior = wl["prior"] if isinstance(wl["prior"], list) else [wl["prior"]] * B
-    nseq = min(B, 2)
+
+def oracle_baseline(wl, budget_s: float = 10.0, max_units: int = 64, max_steps: int = 64):
+    """Times the oracle on the GPU machine's host cores over a bounded sample of
+    the workload: layer 0 of the first sequences, every kv head of each, as
+    (sequence, kv head) work units (inputs generated here, untimed). First one
+    single-threaded worker runs all units step after step until ~budget_s
+    have passed (at most max_steps steps); then one single-threaded worker
+    per host core runs the same steps of the units dealt out among them
+    (spawned processes; numpy / BLAS held to one thread each). Returns both
+    throughputs (KV GB/s over the units' algorithmic bytes; decode tokens/s of
+    whole steps, i.e. layer 0's rate divided by the layers a step runs), the
+    worker count and the sample."""
+    import multiprocessing as mp
+    from paged_kv_cache_56_gb300 import synth
+    Hq, Hkv, d = wl["Hq"], wl["Hkv"], wl["d"]
+    G = Hq // Hkv
+    ctxs = _oracle_contexts(wl)
+    nseq = min(len(ctxs), max(1, max_units // Hkv))
     mult = lambda kind: (synth.outlier_multipliers(SEED, 0, kind, Hkv, d) if wl["outliers"] else
                          synth.head_multipliers(SEED, 0, kind, Hkv) if wl["head_scale"] else None)
-    hists = []
-    for i in range(nseq):
-        h = SequenceHistory(Hkv, d, bs, wl["int8"])
-        pos = torch.arange(prior[i])
-        h.append(synth.kv_rows(SEED, 0, synth.KIND_K, 1000 + i, pos, Hkv, d, mult=mult(synth.KIND_K)).float().numpy(),
-                 synth.kv_rows(SEED, 0, synth.KIND_V, 1000 + i, pos, Hkv, d, mult=mult(synth.KIND_V)).float().numpy())
-        hists.append(h)
-    sm = 1.0 / math.sqrt(d)
     qm = synth.head_multipliers(SEED, 0, synth.KIND_Q, Hq) if wl["head_scale"] else None
-    done_bytes, done_tokens, t_used = 0, 0, 0.0
-    for s in range(steps):
-        for i, h in enumerate(hists):
-            p = torch.tensor([h.n])
-            kr = synth.kv_rows(SEED, 0, synth.KIND_K, 1000 + i, p, Hkv, d, mult=mult(synth.KIND_K)).float().numpy()
-            vr = synth.kv_rows(SEED, 0, synth.KIND_V, 1000 + i, p, Hkv, d, mult=mult(synth.KIND_V)).float().numpy()
-            q = synth.q_rows(SEED, 0, s, [1000 + i], Hq, d, mult=qm)[0].float().numpy()
-            t0 = time.perf_counter()
-            h.append(kr, vr)
-            k, v = h.context()
-            decode_attention(q, k, v, sm)
-            t_used += time.perf_counter() - t0
-            done_bytes += attention_bytes([h.n], Hq, Hkv, d, bs, wl["int8"])
-            done_tokens += 1
-        if t_used > budget_s:
-            break
-    cores = torch.get_num_threads()
-    sample = (f"{s + 1} decode step(s) of {nseq} sequence(s) of one layer (all {Hq} query heads), "
-              f"context ~{max(prior[:nseq])}; scaled per byte")
-    return done_bytes / t_used / 1e9, done_tokens / t_used, sample, cores, t_used
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    units = []
+    for b in range(nseq):
+        n, rid = ctxs[b], 1000 + b
+        pos = torch.arange(n + max_steps)
+        k = bits(synth.kv_rows(SEED, 0, synth.KIND_K, rid, pos, Hkv, d, mult=mult(synth.KIND_K)))
+        v = bits(synth.kv_rows(SEED, 0, synth.KIND_V, rid, pos, Hkv, d, mult=mult(synth.KIND_V)))
+        q = bits(synth.q_rows(SEED, 0, torch.arange(max_steps), [rid] * max_steps, Hq, d, mult=qm))
+        for h in range(Hkv):
+            units.append((n, np.ascontiguousarray(k[:, h]), np.ascontiguousarray(v[:, h]),
+                          np.ascontiguousarray(q[:, h * G:(h + 1) * G])))
+    meta = dict(d=d, bs=wl["bs"], int8=wl["int8"], G=G)
+    cores = os.cpu_count() or 1
+    workers = min(cores, len(units))
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers, initializer=_pool_init, initargs=(ctx.Barrier(workers),)) as pool:
+            t1, steps, b1, _ = pool.apply(_oracle_task, ((meta, units, max_steps, budget_s, False),))
+            res = pool.map(_oracle_task, [(meta, units[i::workers], steps, None, True) for i in range(workers)],
+                           chunksize=1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    tn = max(r[0] for r in res)
+    bn = sum(r[2] for r in res)
+    tokens = nseq * steps / (wl["L"] * wl["repeat"])  # whole decode steps: all layers (and repeats)
+    sample = (f"{steps} decode step(s) of layer 0 for {len(units)} (sequence, kv head) units "
+              f"({nseq} sequence(s), contexts {min(ctxs[:nseq])}-{max(ctxs[:nseq])} tokens), every query head of "
+              f"each unit's group; scaled per byte")
+    return dict(single_gbs=b1 / t1 / 1e9, single_s=t1, all_gbs=bn / tn / 1e9, all_s=tn, workers=workers,
+                cpu_count=cores, steps=steps, sample=sample, all_tokens_per_s=tokens / tn,
+                single_tokens_per_s=tokens / t1)
+
+
+def cpu_baseline_entry(r: dict) -> dict:
+    """The bench line's cpu_baseline object from oracle_baseline's result."""
+    return {"value": round(r["all_gbs"], 4), "unit": "GB/s", "cores": r["workers"], "kind": "oracle",
+            "sample": r["sample"], "seconds": round(r["all_s"], 2),
+            "tokens_per_s": round(r["all_tokens_per_s"], 3), "host_cpu_count": r["cpu_count"],
+            "single_thread": {"value": round(r["single_gbs"], 4), "unit": "GB/s", "cores": 1,
+                              "seconds": round(r["single_s"], 2),
+                              "tokens_per_s": round(r["single_tokens_per_s"], 3)}}
 
 
 # ---------------------------------------------------------------------------
@@ -515,15 +598,15 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        gbs, tps, sample, cores, used = oracle_sample(wl, steps=args.warmup + args.steps, budget_s=60.0)
+        r = oracle_baseline(wl, budget_s=20.0)
+        gbs, tps = r["all_gbs"], r["all_tokens_per_s"]
         line = {"impl": "reference", "metric": "paged decode-attention KV GB/s", "value": round(gbs, 4),
                 "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded counter-based generator)",
                 "config": {"workload": args.workload, "desc": wl["desc"]},
                 "tokens_per_s": round(tps, 3),
-                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                 "sample": sample, "seconds": round(used, 2)},
+                "cpu_baseline": cpu_baseline_entry(r),
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -583,9 +666,7 @@ def main():
         "e2e": r["e2e"],
     }
     if not args.no_cpu_baseline:
-        gbs, tps, sample, cores, used = oracle_sample(wl, steps=1000, budget_s=15.0)
-        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": sample, "seconds": round(used, 2), "tokens_per_s": round(tps, 3)}
+        line["cpu_baseline"] = cpu_baseline_entry(oracle_baseline(wl, budget_s=10.0))
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
