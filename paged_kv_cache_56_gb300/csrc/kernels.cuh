@@ -29,6 +29,7 @@
 //     before waiting for the previous kernel.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -65,6 +66,11 @@ __device__ __forceinline__ void report(int32_t* err, int bits) {
 }
 
 struct DecodeParams {
+    // tensor maps of the K and V pools seen as bytes [num_blocks][Hkv*bs][row],
+    // 128-byte x 16-row boxes with the 128-byte swizzle (used when a token row
+    // is 128 or 256 bytes; unused for 64-byte rows)
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
     const void* k_pool;
     const void* v_pool;
     const float* scales;
@@ -94,13 +100,26 @@ struct DecodeTraits {
     static constexpr int kTileBytes = kTile * kRowBytes;  // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kStages = INT8 ? PKV_STAGES_INT8 : PKV_STAGES_BF16;
+    // Rows of 128 or 256 bytes are staged by tensor copies with the 128-byte
+    // swizzle: each 128-byte half of a row goes to its own 2048-byte slab
+    // (16 rows x 128 bytes), whose 16-byte chunk c of row r sits at chunk
+    // position c ^ (r % 8) -- the eight rows a quarter-warp reads then hit
+    // eight different bank groups. 64-byte rows (INT8, d = 64) are copied
+    // linearly.
+    static constexpr bool kSwz = kRowBytes >= 128;
+    // bf16 at d = 128 (256-byte rows, two slabs): the lanes' dims are
+    // interleaved over the two halves of a row (see the tile math below).
+    static constexpr bool kHalves = !INT8 && D == 128;
+    // slack to align the stages to 1024 bytes (the swizzle pattern's period)
+    static constexpr int kAlignSlack = kSwz ? 1024 : 0;
 };
 
 // Shared-memory bytes of a decode CTA before its block table.
 template <int D, bool INT8>
 constexpr size_t decode_smem_fixed() {
     using T = DecodeTraits<D, INT8>;
-    return size_t(kWarps) * T::kStages * T::kStageBytes   // stages (and, after the loop, the merge)
+    return size_t(T::kAlignSlack)                         // alignment of the stages
+         + size_t(kWarps) * T::kStages * T::kStageBytes   // stages (and, after the loop, the merge)
          + size_t(kWarps) * T::kStages * 8;               // mbarriers
 }
 
@@ -116,6 +135,12 @@ constexpr size_t decode_smem_fixed() {
 // V operand: m-tile m's rows are dims g*D/8 + 2m (row g) and g*D/8 + 2m + 1
 // (row g+8), so lane g reads the contiguous run [g*D/8, g*D/8 + D/8) of
 // tokens 2t, 2t+1, 2t+8, 2t+9; the output row of a lane is that run too.
+// HALVES (bf16, d = 128: 256-byte rows staged as two 128-byte slabs): the
+// runs are split over the two halves of the row instead -- lane t's K dims
+// are [16t, 16t+16) and [64+16t, 64+16t+16), lane g's V dims [8g, 8g+8) and
+// [64+8g, 64+8g+8) -- so that with the swizzle the 16-byte loads of a
+// quarter-warp (g in {2i, 2i+1}, t in 0..3) fall in eight different chunk
+// positions, for K (chunk 2t + c ^ g) and for V (chunk g ^ row) alike.
 // P^T comes from S by an in-register 8x8 transpose (movmatrix).
 // INT8 codes are exact in f16 (x + 1152 = f16 bits 0x6400 | (x ^ 0x80), then
 // subtract 1152); bf16 caches multiply in bf16.
@@ -196,6 +221,15 @@ struct SmemRows {
         return v;
     }
 };
+// A tile staged by tensor copies with the 128-byte swizzle (1024-byte
+// aligned): byte `off` of row r lies in slab off / 128, at chunk position
+// ((off % 128) / 16) ^ (r % 8) of that row.
+struct SwzRows {
+    uint32_t base;
+    __device__ __forceinline__ uint4 ld16(int r, int off) const {
+        return lds128(base + uint32_t((off >> 7) * 2048 + r * 128 + ((((off >> 4) & 7) ^ (r & 7)) << 4)));
+    }
+};
 struct GmemRows {  // rows this kernel may itself have written: read through L2
     const uint8_t* base;
     int row;
@@ -205,17 +239,31 @@ struct GmemRows {  // rows this kernel may itself have written: read through L2
     }
 };
 
-template <int NB, class Rows>
-__device__ __forceinline__ void load_run(const Rows& R, int r, int off, uint32_t* w) {
+// Byte offset in a row of the c-th 16-byte chunk of a lane's K run (lane t)
+// or V run (lane g), NB bytes long; HALVES splits the run over the two
+// 128-byte halves of the row (see the tile math above).
+template <int NB, bool HALVES>
+__device__ __forceinline__ int k_chunk(int t, int c) {
+    return HALVES ? (c >> 1) * 128 + t * (NB / 2) + (c & 1) * 16 : t * NB + c * 16;
+}
+template <int NB, bool HALVES>
+__device__ __forceinline__ int v_chunk(int g, int c) {
+    return HALVES ? c * 128 + g * (NB / 2) : g * NB + c * 16;
+}
+
+// The NB bytes of a lane's run in row r: 16-byte chunks at chunk(c), or one
+// 8-byte piece at chunk(0).
+template <int NB, class Rows, class Chunk>
+__device__ __forceinline__ void load_run(const Rows& R, int r, Chunk chunk, uint32_t* w) {
     if constexpr (NB % 16 == 0) {
 #pragma unroll
         for (int c = 0; c < NB / 16; ++c) {
-            const uint4 v = R.ld16(r, off + c * 16);
+            const uint4 v = R.ld16(r, chunk(c));
             w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
         }
     } else {
         static_assert(NB == 8, "8- or 16k-byte runs");
-        const uint2 v = R.ld8(r, off);
+        const uint2 v = R.ld8(r, chunk(0));
         w[0] = v.x; w[1] = v.y;
     }
 }
@@ -240,8 +288,8 @@ __device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) 
 // hs[j]: log2-domain logit factor of head 2t+j; ksc: the block's K scale;
 // vmul: factor on the softmax weights before the PV product (the block's V
 // scale for INT8 tiles). SHIFT: weights against st.md (see WarpState), with
-// md kept at m - delta.
-template <int D, bool I8, bool SHIFT, class Rows>
+// md kept at m - delta. HALVES: the lanes' dims split over the row's halves.
+template <int D, bool I8, bool SHIFT, bool HALVES, class Rows>
 __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvalid, float ksc, float vmul,
                                          float delta, const uint32_t (&qf)[D / 16][2], const float (&hs)[2],
                                          int g, int t, WarpState<D>& st) {
@@ -252,8 +300,9 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
     {
         float s2[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t k0[Gm::kKW], k1[Gm::kKW];
-        load_run<Gm::kKB>(K, g, t * Gm::kKB, k0);
-        load_run<Gm::kKB>(K, g + 8, t * Gm::kKB, k1);
+        const auto kc = [t](int c) { return k_chunk<Gm::kKB, HALVES>(t, c); };
+        load_run<Gm::kKB>(K, g, kc, k0);
+        load_run<Gm::kKB>(K, g + 8, kc, k1);
 #pragma unroll
         for (int ks = 0; ks < Gm::kSteps; ++ks) {
             uint32_t a0, a1, a2, a3;
@@ -320,10 +369,11 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
     }
     // ---- O^T += V^T . P^T
     uint32_t v0[Gm::kVW], v1[Gm::kVW], v2[Gm::kVW], v3[Gm::kVW];
-    load_run<Gm::kVB>(V, 2 * t, g * Gm::kVB, v0);
-    load_run<Gm::kVB>(V, 2 * t + 1, g * Gm::kVB, v1);
-    load_run<Gm::kVB>(V, 2 * t + 8, g * Gm::kVB, v2);
-    load_run<Gm::kVB>(V, 2 * t + 9, g * Gm::kVB, v3);
+    const auto vc = [g](int c) { return v_chunk<Gm::kVB, HALVES>(g, c); };
+    load_run<Gm::kVB>(V, 2 * t, vc, v0);
+    load_run<Gm::kVB>(V, 2 * t + 1, vc, v1);
+    load_run<Gm::kVB>(V, 2 * t + 8, vc, v2);
+    load_run<Gm::kVB>(V, 2 * t + 9, vc, v3);
     if (!full) {
 #pragma unroll
         for (int i = 0; i < Gm::kVW; ++i) {
@@ -354,15 +404,16 @@ __device__ __forceinline__ void mma_tile(const Rows& K, const Rows& V, int nvali
 }
 
 // The query words behind a lane's Q^T fragments (head g, zero for g >= G):
-// dims t*D/4 .. t*D/4 + D/4 - 1 of the query row, read through L2 (the row is
-// written by the kernel this one waits for).
-template <int D, int G>
+// dims t*D/4 .. t*D/4 + D/4 - 1 of the query row (HALVES: the split run of
+// the K operand), read through L2 (the row is written by the kernel this one
+// waits for).
+template <int D, int G, bool HALVES>
 __device__ __forceinline__ void load_q_words(const uint16_t* qrow, int g, int t, uint32_t (&w)[D / 8]) {
     constexpr int NW = D / 8;  // bf16 words in a lane's D/4 dims
     if (g < G) {
 #pragma unroll
         for (int c = 0; c < NW / 4; ++c) {
-            const uint4 v = ldcg128(qrow + t * (D / 4) + c * 8);
+            const uint4 v = ldcg128(qrow + k_chunk<D / 2, HALVES>(t, c) / 2);
             w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
         }
     } else {
@@ -530,16 +581,17 @@ constexpr int kExpNone = -1000;
 // sequence b = blockIdx.z). HOOK: the test build of pkv_debug_skip_copy, which
 // can leave one bulk copy unissued.
 template <int D, int G, bool INT8, bool SPLIT, bool HOOK>
-__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
     using T = DecodeTraits<D, INT8>;
     using Gm = Geom<D, INT8>;
     constexpr int STAGES = T::kStages;
+    constexpr bool HALVES = T::kHalves;
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
     const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    uint8_t* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * STAGES * T::kStageBytes);
+    uint8_t* stages = smem + (T::kSwz ? (1024u - (smem_addr(smem) & 1023u)) & 1023u : 0u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stages + size_t(kWarps) * STAGES * T::kStageBytes);
     int32_t* tab = reinterpret_cast<int32_t*>(bars + kWarps * STAGES);
     float2* bsc = reinterpret_cast<float2*>(tab + p.tab_cap);
     // Cross-warp merge space: warp w's o [G][D] and (m, l) [G][2], in its own
@@ -612,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
+    if (T::kSwz && tid == 0) {
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+    }
     auto issue = [&](int tile, int s) {
         const int tok = t0 + tile * kTile;
         const int id = tab[tok / p.bs - blk0];
@@ -621,12 +677,23 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
             mbar_arrive(bar);
             return;
         }
-        const size_t row = (size_t(id) * p.Hkv + kvh) * p.bs + (tok % p.bs);
-        const uint8_t* ks = static_cast<const uint8_t*>(p.k_pool) + row * T::kRowBytes;
-        const uint8_t* vs = static_cast<const uint8_t*>(p.v_pool) + row * T::kRowBytes;
         mbar_arrive_expect_tx(bar, T::kStageBytes);
-        bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
-        bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
+        if constexpr (T::kSwz) {
+            // boxes of 16 rows x 128 bytes at x = 0 (and 128): rows kvh*bs +
+            // tok % bs .. + 15 of block id, inside the block as bs % 16 == 0
+            const int y = kvh * p.bs + tok % p.bs;
+#pragma unroll
+            for (int h = 0; h < T::kRowBytes / 128; ++h) {
+                tma_load_3d(stage_of(s) + h * 2048, &p.tm_k, h * 128, y, id, bar, pol);
+                tma_load_3d(stage_of(s) + T::kTileBytes + h * 2048, &p.tm_v, h * 128, y, id, bar, pol);
+            }
+        } else {
+            const size_t row = (size_t(id) * p.Hkv + kvh) * p.bs + (tok % p.bs);
+            const uint8_t* ks = static_cast<const uint8_t*>(p.k_pool) + row * T::kRowBytes;
+            const uint8_t* vs = static_cast<const uint8_t*>(p.v_pool) + row * T::kRowBytes;
+            bulk_g2s(stage_of(s), ks, T::kTileBytes, bar, pol);
+            bulk_g2s(stage_of(s) + T::kTileBytes, vs, T::kTileBytes, bar, pol);
+        }
     };
     // block scales, copied asynchronously (waited for before the main loop)
     auto load_scales = [&](int lo, int hi) {
@@ -657,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
     // the query: loaded first, so that its latency overlaps the update below
     const uint16_t* qbase = p.q + (size_t(b) * p.Hq + size_t(kvh) * G) * D;
     uint32_t qw[D / 8];
-    load_q_words<D, G>(qbase + size_t(g) * D, g, t, qw);
+    load_q_words<D, G, HALVES>(qbase + size_t(g) * D, g, t, qw);
 
     // ---- fused step update: the split holding token ctx-1 writes that token's
     // K/V row (given in k_new / v_new) and, in INT8 mode, quantizes its block if
@@ -693,11 +760,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         for (int jj = 0; jj < 2; ++jj) {
             const int h = 2 * t + jj;
             if (h < G) {
-                float* dst = o + h * D + g * (D / 8);
+                float* dst = o + h * D;
 #pragma unroll
                 for (int m = 0; m < D / 16; ++m) {
-                    dst[2 * m] = w.acc[m][jj] * units;
-                    dst[2 * m + 1] = w.acc[m][2 + jj] * units;
+                    // dims of m-tile m's rows g and g+8 (see the tile math)
+                    const int d0 = HALVES ? (m >> 2) * (D / 2) + g * 8 + 2 * (m & 3) : g * (D / 8) + 2 * m;
+                    dst[d0] = w.acc[m][jj] * units;
+                    dst[d0 + 1] = w.acc[m][2 + jj] * units;
                 }
                 if (g == 0) {
                     ml[h * 2] = w.m[jj];
@@ -734,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
         const size_t rbase = (size_t(slot) * p.Hkv + kvh) * p.bs + (tail_lo - nfull) + tt * kTile;
         const GmemRows kr{static_cast<const uint8_t*>(p.k_tail) + rbase * D * 2, D * 2};
         const GmemRows vr{static_cast<const uint8_t*>(p.v_tail) + rbase * D * 2, D * 2};
-        mma_tile<D, false, INT8>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, 0.f, qb, hb, g, t, st);
+        mma_tile<D, false, INT8, false>(kr, vr, min(kTile, ntail - tt * kTile), 1.f, 1.f, 0.f, qb, hb, g, t, st);
     }
 
     uint32_t qf[D / 16][2];
@@ -795,8 +864,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const Decode
             ksc = sc.x;
             vmul = sc.y;
         }
-        const SmemRows kr{stage_of(s), Gm::kRow}, vr{stage_of(s) + T::kTileBytes, Gm::kRow};
-        mma_tile<D, INT8, INT8>(kr, vr, nvalid, ksc, vmul, delta, qf, hs, g, t, st);
+        if constexpr (T::kSwz) {
+            const SwzRows kr{stage_of(s)}, vr{stage_of(s) + T::kTileBytes};
+            mma_tile<D, INT8, INT8, HALVES>(kr, vr, nvalid, ksc, vmul, delta, qf, hs, g, t, st);
+        } else {
+            const SmemRows kr{stage_of(s), Gm::kRow}, vr{stage_of(s) + T::kTileBytes, Gm::kRow};
+            mma_tile<D, INT8, INT8, false>(kr, vr, nvalid, ksc, vmul, delta, qf, hs, g, t, st);
+        }
         __syncwarp();
         const int nxt = tile + STAGES * kWarps;
         if (lane == 0 && nxt < nt) {

@@ -4,11 +4,13 @@
 // stream and never allocates device memory.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdint>
+#include <cstring>
 #include <utility>
 
 #include <nvtx3/nvToolsExt.h>
@@ -224,6 +226,55 @@ static int allow_smem(DecodeFn fn, int index, size_t smem) {
     return PKV_OK;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (no link against the driver library); nullptr if unavailable.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return PFN_cuTensorMapEncodeTiled_v12000(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// The decode kernel's tensor map of a pool: the pool as bytes
+// [num_blocks][rows = Hkv * bs][row_bytes], boxes of 16 rows x 128 bytes,
+// 128-byte swizzle. Encoding is host-only work; the last map of each pool is
+// kept per thread (a small direct-mapped cache keyed by the pool's shape).
+static int pool_tensor_map(const void* pool, int32_t num_blocks, int32_t rows, int32_t row_bytes, CUtensorMap* out) {
+    struct Entry {
+        CUtensorMap map;
+        const void* pool;
+        int32_t num_blocks, rows, row_bytes;
+    };
+    thread_local Entry cache[128] = {};
+    const uint64_t h = (uint64_t(reinterpret_cast<uintptr_t>(pool)) >> 8) * 0x9E3779B97F4A7C15ull;
+    Entry& e = cache[h >> 57];
+    if (e.pool != pool || e.num_blocks != num_blocks || e.rows != rows || e.row_bytes != row_bytes) {
+        const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (!enc) return PKV_ERR_CUDA;
+        const cuuint64_t dims[3] = {cuuint64_t(row_bytes), cuuint64_t(rows), cuuint64_t(num_blocks)};
+        const cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(rows) * cuuint64_t(row_bytes)};
+        const cuuint32_t box[3] = {128, 16, 1};
+        const cuuint32_t elem[3] = {1, 1, 1};
+        e.pool = nullptr;
+        if (enc(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, elem,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+        e.pool = pool;
+        e.num_blocks = num_blocks;
+        e.rows = rows;
+        e.row_bytes = row_bytes;
+    }
+    *out = e.map;
+    return PKV_OK;
+}
+
 // Dynamic shared memory of a decode CTA: rings and mbarriers, the block table
 // (tab_cap entries) and, INT8, the block scales.
 static size_t decode_smem(int d, bool int8, int tab_cap) {
@@ -426,6 +477,15 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;  // too many blocks per CTA: use a split
 
     DecodeParams p;
+    const int32_t row_bytes = c->head_dim * (int8 ? 1 : 2);
+    if (row_bytes >= 128) {  // tiles staged by tensor copies
+        const int32_t rows = c->num_kv_heads * c->block_size;
+        if ((st = pool_tensor_map(c->k_pool, c->num_blocks, rows, row_bytes, &p.tm_k)) != PKV_OK) return st;
+        if ((st = pool_tensor_map(c->v_pool, c->num_blocks, rows, row_bytes, &p.tm_v)) != PKV_OK) return st;
+    } else {
+        std::memset(&p.tm_k, 0, sizeof(p.tm_k));
+        std::memset(&p.tm_v, 0, sizeof(p.tm_v));
+    }
     p.k_pool = c->k_pool;
     p.v_pool = c->v_pool;
     p.scales = c->scales;
