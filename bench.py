@@ -587,10 +587,17 @@ def main():
     ap.add_argument("--split", type=int, default=None, help="split_tokens (default: sized to one wave)")
     ap.add_argument("--separate-merge", action="store_true", help="merge split-K partials in a second kernel")
     ap.add_argument("--no-pdl", action="store_true", help="launch kernels without programmatic dependent launch")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run the workload with this many layers (same per-layer launch; for small profiler "
+                         "captures -- the line then names the layer count in config)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = WORKLOADS[args.workload]
+    if args.layers is not None:
+        if args.layers < 1:
+            ap.error("--layers must be >= 1")
+        wl = dict(wl, L=args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     peak, peak_kind = _peaks()
@@ -625,6 +632,7 @@ def main():
                 "vs_baseline": None, "dtype": "int8 KV / bf16 q,out / fp32 accumulate",
                 "data": "synthetic (seeded counter-based generator)",
                 "config": {"workload": "trace", "desc": wl["desc"], "split_tokens": r["split"],
+                           **({"layers": wl["L"]} if args.layers is not None else {}),
                            "timed": "decode kernels of each step (admission prefill excluded)",
                            "running_at_end": r["running"], "finished": r["finished"], "kv_pool_at_end": r["pool"]},
                 "tokens_per_s": round(r["ntok"] / (r["ms"] * 1e-3), 1),
@@ -648,6 +656,7 @@ def main():
         "dtype": "int8 KV / bf16 q,out / fp32 accumulate" if wl["int8"] else "bf16 KV / fp32 accumulate",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": args.workload, "desc": wl["desc"], "split_tokens": r["split"],
+                   **({"layers": wl["L"]} if args.layers is not None else {}),
                    "ctx_range": list(r["ctx"]), "l2": "inputs larger than L2 (per-step KV >> 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "CUDA graph per step" if r["graph"] else "eager",
