@@ -62,16 +62,43 @@ WORKLOADS = {
 SEED = 1234
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace runs collapsed:
+    what the compiler sees, so that editing a comment keeps the hash."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied as is
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the CUDA/C++ sources and the C header (what an ncu capture measured)."""
+    """sha256 over the code (comments and whitespace aside) of the CUDA/C++
+    sources and the C header: what an ncu capture measured."""
     import glob
     import hashlib
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_56_gb300", "csrc", "*")) +
                    glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()
 
 

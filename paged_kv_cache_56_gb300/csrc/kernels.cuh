@@ -6,10 +6,12 @@
 //     the whole GQA group of that kv head, so every KV byte crosses HBM once
 //     per step;
 //   * four warps; each owns a ring of STAGES shared-memory stages and pulls
-//     16-token K and V tiles into them with bulk asynchronous copies (the TMA
-//     engine, one elected lane, completion on an mbarrier), gathering tiles
+//     16-token K and V tiles into them with asynchronous copies of the TMA
+//     engine (one elected lane, completion on an mbarrier), gathering tiles
 //     through the block table. A (block, kv head) tile is contiguous in the
-//     [num_blocks][Hkv][bs][d] pools, so every copy is one linear transfer;
+//     [num_blocks][Hkv][bs][d] pools; rows of 128 or 256 bytes arrive by
+//     tensor copies with the 128-byte swizzle (conflict-free shared-memory
+//     reads), 64-byte rows by one linear copy per tile;
 //   * QK and PV of each 16-token tile run on tensor cores (mma.m16n8k16,
 //     fp32 accumulate) straight from registers: INT8 codes are converted
 //     exactly to f16 in registers, and the per-block scales are applied to

@@ -1,6 +1,6 @@
 // Small inline-PTX helpers for sm_103a: mbarriers, bulk asynchronous
-// global->shared copies (the TMA engine's non-tensor form), shared-memory
-// vector loads and exact int8/bf16 -> fp32 conversions.
+// global->shared copies (the TMA engine's linear and tensor forms),
+// shared-memory vector loads and exact int8/bf16 -> fp32 conversions.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -77,7 +77,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// L2 policy for data read once per step (the KV stream): evict first.
+// ---- tensor (tiled) copy global -> shared ------------------------------------
 // Tensor (tiled) copy of one box of a 3-D tensor map into shared memory,
 // completion on an mbarrier. `tmap` is the generic address of a CUtensorMap
 // held in kernel-parameter space; (x, y, z) is the box's first element, x in
@@ -95,6 +95,7 @@ __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// L2 policy for data read once per step (the KV stream): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
