@@ -342,7 +342,7 @@ int pkv_set_programmatic_launch(int enable);
 /* Test hook for the bounded waits (no counterpart on the pages): with tile
  * >= 0, decode launches issued afterwards run a separately compiled test
  * build of the decode kernel (head_dim 64 only; other shapes then return
- * PKV_ERR_UNSUPPORTED) that leaves the bulk copy of that tile of warp 0 of
+ * PKV_ERR_UNSUPPORTED) that leaves the K/V copies of that tile of warp 0 of
  * its first CTA unissued, so that warp's wait on it runs out (about a
  * second), PKV_DEVERR_TIMEOUT is OR-ed into the error word, and the kernel
  * drains its other copies (each wait again bounded) and returns -- the GPU
