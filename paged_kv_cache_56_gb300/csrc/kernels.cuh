@@ -523,6 +523,83 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Quantize-on-fill inside the decode kernel: the K and V slabs of block `id`
+// (bs rows of D bf16 each) from the slot's bf16 tail rows, except row `off`
+// -- the row this step appends -- which is taken from the new row itself
+// (nrow_k / nrow_v), so the quantizer need not wait for that row's store.
+// Half of the CTA's threads take each slab, 16 rows at a time: a thread
+// holds its chunks of those rows in registers, with all their loads in flight
+// at once. A 16-row block is read once; a larger one is read a second time
+// (from L2) for the codes. The arithmetic is quantize_slab's (absmax, IEEE
+// scale = max/127, round-half-even, clamp to +-127): the same bits.
+template <int D>
+__device__ __forceinline__ void fill_quantize(const DecodeParams& p, const uint16_t* tail_k, const uint16_t* tail_v,
+                                              const uint16_t* nrow_k, const uint16_t* nrow_v, int off, int id,
+                                              int kvh) {
+    constexpr int CH = D / 8;              // 16-byte chunks per row
+    constexpr int TPS = kThreads / 2;      // threads per slab
+    static_assert((kTile * CH) % TPS == 0, "16 rows' chunks split evenly over a slab's threads");
+    constexpr int NB = kTile * CH / TPS;   // chunks a thread holds per 16 rows
+    __shared__ float s_mx[kWarps];
+    const int tid = threadIdx.x, kv = tid / TPS, t = tid % TPS, warp = tid >> 5, lane = tid & 31;
+    const int npass = p.bs / kTile;
+    const uint16_t* tail = kv ? tail_v : tail_k;
+    const uint16_t* nrow = kv ? nrow_v : nrow_k;
+    uint4 w[NB];
+    auto load = [&](int pass) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int c = pass * kTile * CH + t + i * TPS, r = c / CH, ch = c % CH;
+            w[i] = r == off ? ldg128(nrow + ch * 8) : ldcg128(tail + size_t(r) * D + ch * 8);
+        }
+    };
+    float mx = 0.f;
+    for (int pass = 0; pass < npass; ++pass) {
+        load(pass);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = bf16x2_to_f2(ws[k]);
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    if (lane == 0) s_mx[warp] = mx;
+    __syncthreads();
+    constexpr int WPS = TPS / 32;  // warps per slab
+    mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < WPS; ++k) mx = fmaxf(mx, s_mx[kv * WPS + k]);
+    const float scale = mx < 1e-6f ? 1.0f : __fdiv_rn(mx, 127.0f);
+    int8_t* dst = static_cast<int8_t*>(const_cast<void*>(kv ? p.v_pool : p.k_pool)) +
+                  (size_t(id) * p.Hkv + kvh) * p.bs * D;
+    for (int pass = 0; pass < npass; ++pass) {
+        if (npass > 1) load(pass);  // one pass: still held from the maximum
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int c = pass * kTile * CH + t + i * TPS;
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = bf16x2_to_f2(ws[k]);
+                int q0 = __float2int_rn(__fdiv_rn(f.x, scale));
+                int q1 = __float2int_rn(__fdiv_rn(f.y, scale));
+                q0 = min(127, max(-127, q0));
+                q1 = min(127, max(-127, q1));
+                const uint32_t pair = (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8);
+                packed[k >> 1] |= pair << (16 * (k & 1));
+            }
+            *reinterpret_cast<uint2*>(dst + size_t(c) * 8) = make_uint2(packed[0], packed[1]);
+        }
+    }
+    if (t == 0) const_cast<float*>(p.scales)[(size_t(id) * p.Hkv + kvh) * 2 + kv] = scale;
+}
+
 // The step update of (sequence b, kv head kvh) whose context now ends at
 // token ctx-1: writes that token's K/V row (k_new / v_new) into the cache --
 // the slot's bf16 tail (INT8) or pool block `id` (bf16) -- and, in INT8 mode,
@@ -531,7 +608,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
 template <int D, bool INT8>
 __device__ __forceinline__ void step_update(const DecodeParams& p, const int b, const int kvh, const int ctx,
                                             const int id) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int pos = ctx - 1, off = pos % p.bs;
     const int slot = (INT8 && p.slots) ? p.slots[b] : -1;
     const bool ok = INT8 ? (slot >= 0 && slot < p.max_slots) : (id >= 0);
@@ -549,23 +626,20 @@ __device__ __forceinline__ void step_update(const DecodeParams& p, const int b, 
     } else if (tid == 0) {
         report(p.err, INT8 ? kErrSlot : kErrBlockId);
     }
-    __syncthreads();
-    if (INT8 && ok && (pos + 1) % p.bs == 0) {
+    if (INT8 && ok && (pos + 1) % p.bs == 0) {  // the row filled block id
         if (id >= 0) {
-            for (int kv = warp; kv < 2; kv += kWarps) {  // K slab, V slab
-                const uint16_t* src = static_cast<const uint16_t*>(kv ? p.v_tail : p.k_tail) +
-                                      (size_t(slot) * p.Hkv + kvh) * p.bs * D;
-                int8_t* dst = static_cast<int8_t*>(const_cast<void*>(kv ? p.v_pool : p.k_pool)) +
-                              (size_t(id) * p.Hkv + kvh) * p.bs * D;
-                quantize_slab<D, true>(lane, src, D, p.bs, dst,
-                                       const_cast<float*>(p.scales) + (size_t(id) * p.Hkv + kvh) * 2 + kv);
-                fence_proxy_async_global();  // the codes are read by a bulk copy later
-            }
+            const size_t t0 = (size_t(slot) * p.Hkv + kvh) * p.bs * D;
+            const uint16_t* tk = static_cast<const uint16_t*>(p.k_tail) + t0;
+            const uint16_t* tv = static_cast<const uint16_t*>(p.v_tail) + t0;
+            const uint16_t* nk = p.k_new + (size_t(b) * p.Hkv + kvh) * D;
+            const uint16_t* nv = p.v_new + (size_t(b) * p.Hkv + kvh) * D;
+            fill_quantize<D>(p, tk, tv, nk, nv, off, id, kvh);
+            fence_proxy_async_global();  // the codes are read by a bulk copy later
         } else if (tid == 0) {
             report(p.err, kErrBlockId);
         }
-        __syncthreads();
     }
+    __syncthreads();
 }
 
 // INT8 caches keep the PV accumulators (and l) of a CTA in units of
