@@ -261,7 +261,8 @@ int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* 
                          float* ws_o, float* ws_ml, int32_t* ws_count, void* out, void* stream);
 
 /* One layer's whole decode step in one kernel: for each sequence b, append
- * the new rows k_new[b], v_new[b] ([B][Hkv][d] bf16, device) as token
+ * the new rows k_new[b], v_new[b] ([B][Hkv][d] bf16, device, 16-byte
+ * aligned; PKV_ERR_INVALID otherwise) as token
  * ctx_lens[b] - 1 (BF16: into block block_tables[b][(ctx_lens[b]-1)/bs],
  * which must already be allocated; INT8: into the tail of slots[b]); in INT8
  * mode, if that token fills its block, quantize the block into the pool
@@ -280,8 +281,9 @@ int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, c
 /* A whole decode step over num_layers layers in one call, layer l after
  * layer l-1 on the stream: layer l runs pkv_decode_step on descs[l] with
  * q + l*q_layer_stride, k_new/v_new + l*kv_layer_stride and
- * out + l*out_layer_stride (strides in bytes, multiples of 16), or
- * pkv_decode_attention when k_new and v_new are both NULL. The block tables,
+ * out + l*out_layer_stride (strides in bytes, multiples of 16; k_new and
+ * v_new 16-byte aligned), or pkv_decode_attention when k_new and v_new are
+ * both NULL (one NULL without the other: PKV_ERR_INVALID). The block tables,
  * context lengths, slots, split settings and workspace are shared by all
  * layers (the layers of a model allocate the same blocks). Stops at, and
  * returns, the first error. */

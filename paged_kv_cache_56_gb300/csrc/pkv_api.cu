@@ -460,6 +460,8 @@ static int decode_impl(const pkv_cache_desc* c, const void* q, const void* k_new
     if (B == 0) return PKV_OK;
     if (!q || !block_tables || !ctx_lens || !out || B > 65535 || c->num_kv_heads > 65535) return PKV_ERR_INVALID;
     if (!aligned16(q) || (reinterpret_cast<uintptr_t>(out) & 3u)) return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;  // 16-byte row loads
     const bool int8 = c->dtype == PKV_DTYPE_INT8;
     if (int8 && !slots) return PKV_ERR_INVALID;
     const int64_t max_ctx = int64_t(max_blocks) * c->block_size;

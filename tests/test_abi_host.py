@@ -97,6 +97,14 @@ def test_argument_validation(L):
     static = L.pkv_decode_attention_static_ws
     assert static(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, -16, 2, 16, None) == pkv.PKV_ERR_INVALID
     assert attn(ctypes.byref(d), 16, 16, 4, 16, 16, 1, 0.1, -16, 2, 16, 16, None, 16, None) == pkv.PKV_ERR_INVALID
+    # appended rows are read 16 bytes at a time: a misaligned k_new / v_new is refused
+    layers = L.pkv_decode_layers
+    assert layers(ctypes.byref(d), 1, 16, 0, 24, 32, 0, 16, 0, 16, 4, 16, 16, 1, 0.1, 0, 0,
+                  None, None, None, None) == pkv.PKV_ERR_INVALID
+    assert layers(ctypes.byref(d), 1, 16, 0, 32, 40, 0, 16, 0, 16, 4, 16, 16, 1, 0.1, 0, 0,
+                  None, None, None, None) == pkv.PKV_ERR_INVALID
+    assert L.pkv_decode_step(ctypes.byref(d), 16, 24, 32, 16, 4, 16, 16, 1, 0.1, 0, 0, None, None, None,
+                             16, None) == pkv.PKV_ERR_INVALID
     # the error-word reader: bad counts and a NULL array are refused before any CUDA call
     bits = ctypes.c_int32(7)
     assert L.pkv_sync_status(None, 1, None, ctypes.byref(bits)) == pkv.PKV_ERR_INVALID
