@@ -221,14 +221,17 @@ def test_pipelined_host_steps_equal_graph_steps(int8):
 
 
 @pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
-@pytest.mark.parametrize("d,bs", [(64, 16), (128, 64)], ids=["d64_bs16", "d128_bs64"])
+@pytest.mark.parametrize("d,bs", [(64, 16), (64, 64), (128, 64)], ids=["d64_bs16", "d64_bs64", "d128_bs64"])
 @pytest.mark.parametrize("split", [0, 64])
-def test_gqa_group_of_eight(int8, d, bs, split):
+@pytest.mark.parametrize("fused", [False, True], ids=["three_kernels", "fused_step"])
+def test_gqa_group_of_eight(int8, d, bs, split, fused):
     """The widest GQA group the kernels take (G = Hq / Hkv = 8, the MMA's full
     N dimension), both head sizes and block sizes, with and without splits,
-    across block fills, against the oracle."""
+    across block fills (the sequence of 63 tokens fills a 64-token block at
+    the first step: with fused_step, the decode kernel's own quantize-on-fill
+    of a 64-row slab), against the oracle and byte for byte in the pools."""
     w = Workload(seed=70 + d + bs, num_layers=1, prior=(3, 63, 64, 130), Hq=16, Hkv=2, d=d, bs=bs, num_blocks=40,
-                 int8=int8, split_tokens=split, max_blocks=5 if bs == 64 else 14)
+                 int8=int8, split_tokens=split, max_blocks=5 if bs == 64 else 14, fused_step=fused)
     for t in range(20):
         out = w.step().float().cpu().numpy()
         if t in (0, 1, 19):
