@@ -206,10 +206,17 @@ class TraceDriver:
         return rids, plan
 
     def batch_order(self) -> list:
-        """Running request ids in the order the step batches them: longest
-        context first. The decode grid starts its CTAs in batch order, so the
-        longest sequences start first and the short ones fill in behind them."""
-        return [r.rid for r in sorted(self.running, key=lambda r: -r.length)]
+        """Running request ids in the order the step batches them. The decode
+        grid starts its CTAs in batch order. The shortest quarter of the
+        requests goes first, shortest first: their CTAs do little streaming
+        and mostly wait on their start-up loads (context, table, query, tail),
+        so they are best started while the previous layer drains and finished
+        early, instead of ending the layer. The rest follow longest first, so
+        the long sequences start at once and the others fill in behind them."""
+        rs = sorted(self.running, key=lambda r: -r.length)
+        k = len(rs) // 4
+        rs = rs[len(rs) - k:][::-1] + rs[:len(rs) - k]
+        return [r.rid for r in rs]
 
     def _new_rows(self, layer: int, kind: int, rids, positions) -> torch.Tensor:
         c = self.cache

@@ -1,7 +1,7 @@
 """The continuous-batching trace (200 decode steps, up to 128 running
 requests, Hq=32, Hkv=8, d=128, 16-token blocks, INT8 cache, 32 layers, a
 200-token shared prefix), in the launch configuration the benchmark times
-(its split length, programmatic dependent launch, longest context first):
+(its split length, programmatic dependent launch, the driver's batch order):
 sampled outputs against the oracle every 20th step, block conservation every
 step, and the pools of sampled requests byte for byte at the end."""
 
