@@ -39,10 +39,10 @@
 #include "ptx.cuh"
 
 #ifndef PKV_STAGES_INT8
-#define PKV_STAGES_INT8 2  // bulk-copy stages per warp, INT8 cache (4 KB each at d = 128)
+#define PKV_STAGES_INT8 2  // TMA-copy stages per warp, INT8 cache (4 KB each at d = 128)
 #endif
 #ifndef PKV_STAGES_BF16
-#define PKV_STAGES_BF16 2  // bulk-copy stages per warp, bf16 cache (8 KB each at d = 128)
+#define PKV_STAGES_BF16 2  // TMA-copy stages per warp, bf16 cache (8 KB each at d = 128)
 #endif
 
 namespace pkv {
@@ -622,7 +622,7 @@ __device__ __forceinline__ void step_update(const DecodeParams& p, const int b, 
             const int kv = c / (D / 8), ch = c % (D / 8);
             *reinterpret_cast<uint4*>((kv ? dv : dk) + ch * 8) = ldg128((kv ? sv : sk) + ch * 8);
         }
-        if (!INT8) fence_proxy_async_global();  // the pool row is read by a bulk copy later
+        if (!INT8) fence_proxy_async_global();  // the pool row is read by a TMA copy later
     } else if (tid == 0) {
         report(p.err, INT8 ? kErrSlot : kErrBlockId);
     }
@@ -634,7 +634,7 @@ __device__ __forceinline__ void step_update(const DecodeParams& p, const int b, 
             const uint16_t* nk = p.k_new + (size_t(b) * p.Hkv + kvh) * D;
             const uint16_t* nv = p.v_new + (size_t(b) * p.Hkv + kvh) * D;
             fill_quantize<D>(p, tk, tv, nk, nv, off, id, kvh);
-            fence_proxy_async_global();  // the codes are read by a bulk copy later
+            fence_proxy_async_global();  // the codes are read by a TMA copy later
         } else if (tid == 0) {
             report(p.err, kErrBlockId);
         }
@@ -655,7 +655,7 @@ constexpr int kExpNone = -1000;
 
 // Decode attention, one CTA per (split j = blockIdx.x, kv head = blockIdx.y,
 // sequence b = blockIdx.z). HOOK: the test build of pkv_debug_skip_copy, which
-// can leave one bulk copy unissued.
+// can leave one tile's copies unissued.
 template <int D, int G, bool INT8, bool SPLIT, bool HOOK>
 __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide N dimension");
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) decode_kernel(const __grid
 
     // ---- INT8: the partly filled last block, read from the slot's bf16 tail.
     // Done before the pool tiles, so that its global loads overlap the ring's
-    // first bulk copies; tail tile tt goes to warp kWarps-1-tt (the warps with
+    // first copies; tail tile tt goes to warp kWarps-1-tt (the warps with
     // the fewest pool tiles), accumulated in plain units (converted to the
     // CTA's units once those are known).
     const int tail_lo = INT8 ? max(t0, nfull) : 0;

@@ -318,7 +318,7 @@ def pkv_quantize_blocks_from(desc: CacheDesc, k_src: torch.Tensor, v_src: torch.
 
 
 def pkv_debug_skip_copy(tile: int) -> None:
-    """Test hook: later decode launches leave one bulk copy unissued so that a
+    """Test hook: later decode launches leave one tile's copies unissued so that a
     bounded wait runs out (PKV_DEVERR_TIMEOUT); -1 turns it off."""
     _check("pkv_debug_skip_copy", lib().pkv_debug_skip_copy(tile))
 
