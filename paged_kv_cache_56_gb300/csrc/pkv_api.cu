@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <utility>
 
 #include <nvtx3/nvToolsExt.h>
@@ -206,23 +207,27 @@ static DecodeFn pick_decode(int d, int g, bool int8, bool split, bool hook, int*
 }
 
 // Raises the kernel's dynamic shared-memory limit (once per kernel, device
-// and size) so that it can be launched or sized with `smem` bytes.
+// and size) so that it can be launched or sized with `smem` bytes. Safe from
+// several host threads: the limit is only ever raised, under a lock, and the
+// record of the largest size set is read without one.
 static int allow_smem(DecodeFn fn, int index, size_t smem) {
-    static int configured[64][64] = {};
+    static std::atomic<int> configured[64][64] = {};
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-    if (int(smem) > configured[index][dev]) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem)) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        // all of the unified L1 as shared memory: the kernel streams through
-        // shared memory and gains nothing from L1, and a smaller carveout
-        // would cap the CTAs per SM below what registers allow
-        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured[index][dev] = int(smem);
-    }
+    if (int(smem) <= configured[index][dev].load(std::memory_order_acquire)) return PKV_OK;
+    std::lock_guard<std::mutex> lock(mu);
+    if (int(smem) <= configured[index][dev].load(std::memory_order_relaxed)) return PKV_OK;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    // all of the unified L1 as shared memory: the kernel streams through
+    // shared memory and gains nothing from L1, and a smaller carveout would
+    // cap the CTAs per SM below what registers allow
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    configured[index][dev].store(int(smem), std::memory_order_release);
     return PKV_OK;
 }
 
@@ -613,8 +618,6 @@ int pkv_decode_step(const pkv_cache_desc* c, const void* q, const void* k_new, c
 namespace pkv {
 static __device__ __align__(256) unsigned char g_static_ws[PKV_STATIC_WS_BYTES];
 }  // namespace pkv
-
-#include <mutex>
 
 // Device address of g_static_ws on the current device, looked up once per
 // device (in host code the array's name is only a host-side stand-in).
