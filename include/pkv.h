@@ -254,7 +254,10 @@ int pkv_copy_slots(const pkv_cache_desc* c, const int32_t* src_slots, const int3
  *   ready for the next call (a sequence whose context fits one split writes
  *   its output directly, leaving workspace and counter untouched). Calls
  *   sharing a workspace must not overlap.
- * slots may be NULL in BF16 mode. */
+ * slots may be NULL in BF16 mode. With rows of 128 or 256 bytes (INT8 or bf16
+ * at head_dim 128, bf16 at head_dim 64) the kernel reads the pools through
+ * tensor maps that the call encodes on the host (cached per thread);
+ * PKV_ERR_CUDA if the driver's encoder is unavailable or refuses the pool. */
 int pkv_decode_attention(const pkv_cache_desc* c, const void* q, const int32_t* block_tables,
                          int32_t max_blocks, const int32_t* ctx_lens, const int32_t* slots,
                          int32_t B, float sm_scale, int32_t split_tokens, int32_t max_splits,
